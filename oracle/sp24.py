@@ -1,0 +1,122 @@
+"""2:4 fine-grained structured sparsity: magnitude pruning and compression.
+
+Pattern ("NVIDIA A100 benchmarks" blog page, the paragraph on 2:4 structured
+sparsity and its Figure 1 caption; "Accelerating Sparse Deep Neural Networks",
+Abstract; "Accelerating Sparse DNNs Based on Tiled GEMM", Figure 1 caption):
+in every contiguous block of four values along K, two are zero, and the matrix
+is stored as its nonzero values plus metadata giving their positions.
+
+Readings where the pages are silent (each also listed in the design notes):
+  * criterion: keep the two largest magnitudes of each group (magnitude pruning);
+  * magnitude order is the order of the stored bits with the sign bit cleared
+    (exact for finite values; +0 and -0 compare equal);
+  * ties go to the lower position; an all-equal group keeps positions (0, 1);
+  * groups start at k = 0; K % 4 == 0;
+  * kept values are stored in ascending position order, bits copied (sign of
+    zero kept);
+  * metadata nibble of a group is j0 | j1 << 2 with j0 < j1; nibble g sits in
+    byte g // 2 of its row, low nibble first.
+
+Layouts (the library's contract, restated here from the header):
+  Kp = round_up(K, 32); values are M x Kp/2 elements, meta M x Kp/8 bytes;
+  positions past K hold value 0 and nibble 0x4.
+  meta_hw: blocks of 128 rows x 16 bytes, one block per (128-row block,
+  128-column block of K); block (mb, kb) starts at byte 2048 * (mb * KB + kb),
+  KB = ceil(K / 128), and row r of the block holds the canonical bytes of
+  groups 32 kb .. 32 kb + 31 of row 128 mb + r in order. Rows past M and
+  groups past K hold nibble 0x4.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+PAD_NIBBLE = 0x4
+
+
+def magnitude_key(bits: np.ndarray, dt: str) -> np.ndarray:
+    """Integer whose order is the |value| order of finite values of type dt."""
+    mask = 0x7F if dt == "e4m3" else 0x7FFF
+    return bits.astype(np.int64) & mask
+
+
+def prune_positions(bits: np.ndarray, dt: str) -> tuple[np.ndarray, np.ndarray]:
+    """For W (M x K bits), the two kept positions (j0 < j1) of each group of 4.
+
+    Returns j0, j1 of shape (M, K // 4).
+    """
+    M, K = bits.shape
+    if K % 4:
+        raise ValueError("K must be a multiple of 4")
+    key = magnitude_key(bits, dt).reshape(M, K // 4, 4)
+    # Stable sort of -key: larger magnitudes first; equal magnitudes keep their
+    # position order, so ties go to the lower position.
+    order = np.argsort(-key, axis=-1, kind="stable")
+    top = np.sort(order[..., :2], axis=-1)
+    return top[..., 0], top[..., 1]
+
+
+def prune(bits: np.ndarray, dt: str) -> np.ndarray:
+    """prune(W): W with the two smaller-magnitude entries of each group set to +0 bits."""
+    M, K = bits.shape
+    j0, j1 = prune_positions(bits, dt)
+    keep = np.zeros((M, K // 4, 4), dtype=bool)
+    np.put_along_axis(keep, j0[..., None], True, axis=-1)
+    np.put_along_axis(keep, j1[..., None], True, axis=-1)
+    out = np.where(keep.reshape(M, K), bits, 0).astype(bits.dtype)
+    return out
+
+
+def padded_k(K: int) -> int:
+    return (K + 31) // 32 * 32
+
+
+def compress(bits: np.ndarray, dt: str) -> tuple[np.ndarray, np.ndarray]:
+    """Compressed representation of prune(W): (values M x Kp/2, meta M x Kp/8 bytes)."""
+    M, K = bits.shape
+    Kp = padded_k(K)
+    j0, j1 = prune_positions(bits, dt)
+    g = bits.reshape(M, K // 4, 4)
+    v0 = np.take_along_axis(g, j0[..., None], axis=-1)[..., 0]
+    v1 = np.take_along_axis(g, j1[..., None], axis=-1)[..., 0]
+    values = np.zeros((M, Kp // 2), dtype=bits.dtype)
+    values[:, 0:K // 2:2] = v0
+    values[:, 1:K // 2:2] = v1
+    nib = np.full((M, Kp // 4), PAD_NIBBLE, dtype=np.uint8)
+    nib[:, :K // 4] = (j0 | (j1 << 2)).astype(np.uint8)
+    meta = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    return values, meta
+
+
+def nibbles(meta: np.ndarray, groups: int) -> np.ndarray:
+    """Unpack the first `groups` nibbles of each row of canonical metadata."""
+    lo = meta & 0xF
+    hi = meta >> 4
+    n = np.stack([lo, hi], axis=-1).reshape(meta.shape[0], -1)
+    return n[:, :groups]
+
+
+def decompress(values: np.ndarray, meta: np.ndarray, K: int) -> np.ndarray:
+    """Scatter the kept values into an M x K matrix of +0 bits."""
+    M = values.shape[0]
+    n = nibbles(meta, K // 4).astype(np.int64)
+    j0 = n & 3
+    j1 = (n >> 2) & 3
+    out = np.zeros((M, K // 4, 4), dtype=values.dtype)
+    np.put_along_axis(out, j0[..., None], values[:, 0:K // 2:2][..., None], axis=-1)
+    np.put_along_axis(out, j1[..., None], values[:, 1:K // 2:2][..., None], axis=-1)
+    return out.reshape(M, K)
+
+
+def meta_hw_from_canonical(meta: np.ndarray, M: int, K: int) -> np.ndarray:
+    """Re-block canonical metadata (M x Kp/8 bytes) into the 128 x 16-byte blocks."""
+    MB = (M + 127) // 128
+    KB = (K + 127) // 128
+    pad_byte = PAD_NIBBLE | (PAD_NIBBLE << 4)
+    full = np.full((MB * 128, KB * 16), pad_byte, dtype=np.uint8)
+    full[:M, :meta.shape[1]] = meta           # canonical padding nibbles are already 0x4
+    blocks = full.reshape(MB, 128, KB, 16).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(blocks).reshape(-1)
+
+
+def meta_hw_size(M: int, K: int) -> int:
+    return ((M + 127) // 128) * ((K + 127) // 128) * 2048
