@@ -1,0 +1,153 @@
+/*
+ * ssdnn.h -- C ABI of the structured-sparse weight GEMM library for GB300 (sm_103a).
+ *
+ * The library computes Y = W_sparse . X for pruned fully connected layers and
+ * 1x1 convolutions written as GEMMs, with two weight patterns:
+ *
+ *   2:4 fine-grained sparsity -- in every contiguous group of four weights along
+ *   K two are zero; W is stored as its kept values plus 2-bit positions
+ *   ("NVIDIA A100 benchmarks" blog page, paragraph on 2:4 structured sparsity
+ *   and Figure 1 caption; "Accelerating Sparse Deep Neural Networks", Abstract).
+ *
+ *   Tile-wise (TW) sparsity and its tile-vector-wise (TVW) hybrid -- each tile of
+ *   128 output rows keeps its own subset of K indices, applied where operands are
+ *   fetched from global memory; TVW also applies 2:4 inside the kept indices
+ *   ("Accelerating Sparse DNNs Based on Tiled GEMM", TL;DR, Abstract, Figure 3).
+ *
+ * Conventions (every function):
+ *   - Returns an ssdnn_status; no exception or abort crosses the ABI.
+ *   - Pointers are DEVICE pointers unless the parameter name ends in _host.
+ *     The caller owns and allocates every buffer (the *_sizes functions give the
+ *     sizes); the library allocates no memory.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream); outputs are valid once the stream has reached that point.
+ *   - Matrices are row-major with explicit leading dimensions in ELEMENTS:
+ *       W  M x K   (K contiguous),  X  K x N  (N contiguous),  Y  M x N.
+ *     Base pointers must be 16-byte aligned and leading dimension x element size
+ *     a multiple of 16 bytes; otherwise SSDNN_ERR_UNSUPPORTED.
+ *   - Inputs must be finite. Element types: ssdnn_dtype.
+ *   - A kernel whose internal wait exceeds its bound records it in a per-device
+ *     error word and returns; ssdnn_check_device_error() reports it.
+ *
+ * Readings of the method where the pages are silent (magnitude criterion, tie
+ * rules, layouts, tile height 128) are stated beside each call.
+ */
+#ifndef SSDNN_H
+#define SSDNN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSDNN_F16 = 0, SSDNN_BF16 = 1, SSDNN_E4M3 = 2 } ssdnn_dtype;
+
+typedef enum {
+  SSDNN_OK = 0,
+  SSDNN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, inconsistent counts */
+  SSDNN_ERR_UNSUPPORTED = 2, /* shape / alignment / dtype combination not implemented */
+  SSDNN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+  SSDNN_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired */
+  SSDNN_ERR_DEVICE = 5       /* a kernel recorded an internal error */
+} ssdnn_status;
+
+/* Constant string for a status code. */
+const char* ssdnn_status_str(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int ssdnn_version(void);
+
+/* Synchronizes `stream`, then reads and clears this device's error word.
+ * Returns SSDNN_OK, SSDNN_ERR_TIMEOUT or SSDNN_ERR_DEVICE. */
+int ssdnn_check_device_error(void* stream);
+
+/* ------------------------------------------------------------------ 2:4 ----
+ * Compressed 2:4 layouts (Kp = round_up(K, 32)):
+ *   values   M x Kp/2 elements, row-major: the kept values of each group in
+ *            ascending position order, stored bits copied; zero past K/2.
+ *   meta     M x Kp/8 bytes, row-major: group g = k/4 has nibble j0 | j1 << 2
+ *            (j0 < j1 its kept positions), at byte g/2, low nibble for even g;
+ *            nibble 0x4 past K/4.
+ *   meta_hw  the operand order of the sparse tensor core: 2048-byte blocks of
+ *            128 rows x 16 bytes, block (mb, kb) at index mb * KB + kb.
+ *            e4m3: kb spans 128 columns of K (KB = ceil(K/128)); row r holds the
+ *              canonical bytes 16 kb .. 16 kb + 15 of row 128 mb + r.
+ *            fp16/bf16: kb spans 64 columns (KB = ceil(K/64)); row r holds four
+ *              32-bit words; words 0 and 2 cover the column spans 64 kb .. +31
+ *              and 64 kb + 32 .. +63, words 1 and 3 are zero. Rows are paired
+ *              (r and r ^ 8): for r with bit 3 clear the word is (canonical
+ *              nibbles of groups 0..3 of row r) | (groups 0..3 of row r + 8) << 16;
+ *              for r with bit 3 set it is (groups 4..7 of row r - 8) |
+ *              (groups 4..7 of row r) << 16 (groups counted within the span).
+ *            Rows past M and groups past K hold 0x4 nibbles.
+ * Pruning (the pages state no criterion; reading: magnitude): keep the two
+ * entries of largest |w| per group, |w| ordered by the stored bits with the sign
+ * bit cleared, ties to the lower position. K % 4 == 0 is required.
+ */
+int sp24_sizes(int dt, int64_t M, int64_t K, size_t* values_bytes, size_t* meta_bytes,
+               size_t* meta_hw_bytes);
+
+/* W (M x K, leading dimension ldw) -> values, meta, meta_hw (all three written;
+ * meta may be NULL to skip the canonical copy). */
+int sp24_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, void* values,
+                        uint8_t* meta, uint8_t* meta_hw, void* stream);
+
+/* Y = alpha * decompress(values, meta_hw) . X, fp32 accumulation on the sparse
+ * tensor cores, one round-to-nearest-even conversion to out_dt.
+ * in_dt in {F16, BF16, E4M3}; out_dt in {F16, BF16}. values has the pitch Kp/2
+ * of sp24_prune_compress. ldx >= N, ldy >= N. */
+int sp24_gemm(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+              const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+              void* stream);
+
+/* The dense GEMM of the same kernel family: Y = alpha * W . X. */
+int dense_gemm(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
+               const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, void* stream);
+
+/* ------------------------------------------------------------- TW / TVW ----
+ * Tiles are 128 consecutive rows of W (and Y): tile t = rows 128 t ..; the
+ * number of tiles is nt = ceil(M / 128). keep_counts_host[t] = L_t, 0 <= L_t <= K
+ * (TVW: L_t % 4 == 0). dt in {F16, BF16}.
+ * Selection (reading of the pages): score s_t[k] = fp32 sum over the tile's rows
+ * in ascending order of |w_ik|; the kept set is the first L_t of the order
+ * (score descending, k ascending), listed ascending.
+ * Layouts (R_t = round_up(L_t, 64), P_t = sum_{s<t} R_s, Q_t = P_t / 64):
+ *   offsets   nt + 1 int32: offsets[t] = sum_{s<t} L_s.
+ *   indices   offsets[nt] int32: tile t's kept k, ascending, at offsets[t].
+ *   schedule  4 * nt int32: entries (t, L_t, P_t, Q_t) for the tiles ordered by
+ *             L_t descending, ties by t ascending (tiles of equal length form a
+ *             batch; the GEMM hands out work in this order for load balance).
+ *   packed    TW:  128 * P_nt elements; element (t, r, j), j < R_t, at
+ *                  128 P_t + 8192 (j / 64) + 64 r + j % 64 (zero past L_t and
+ *                  past row M).
+ *             TVW: 64 * P_nt elements, the 2:4 values of each packed tile:
+ *                  (t, r, c), c < R_t / 2, at 64 P_t + 4096 (c / 32) + 32 r + c % 32.
+ *   meta      TVW only: 16 * P_nt bytes; byte b < R_t / 8 of tile row r at
+ *             16 P_t + r R_t / 8 + b (canonical nibbles along the compacted K).
+ *   meta_hw   TVW only: 32 * P_nt bytes; tile t's metadata in the fp16/bf16
+ *             operand order of meta_hw above (128 rows, K = R_t), R_t / 64 blocks
+ *             starting at block Q_t.
+ *   workspace scratch for the scores: nt * K * 4 bytes.
+ */
+int tw_sizes(int dt, int tvw, int64_t M, int64_t K, const int32_t* keep_counts_host,
+             size_t* packed_bytes, size_t* indices_count, size_t* meta_bytes, size_t* meta_hw_bytes,
+             size_t* workspace_bytes);
+
+int tw_prune_compress(int dt, int tvw, const void* W, int64_t M, int64_t K, int64_t ldw,
+                      const int32_t* keep_counts_host, int32_t* offsets, int32_t* indices,
+                      int32_t* schedule, void* packed, uint8_t* meta, uint8_t* meta_hw, void* workspace,
+                      void* stream);
+
+/* Y[tile t rows] = W_t . X[indices of t, :] (TW) or the 2:4 product of the TVW
+ * values (TVW), fp32 accumulation, one RNE conversion to dt. A tile with L_t = 0
+ * writes zeros. keep_counts_host is the array given to tw_prune_compress. */
+int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* keep_counts_host,
+             const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+             const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSDNN_H */

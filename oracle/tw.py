@@ -15,7 +15,8 @@ Readings where the pages are silent (each also listed in the design notes):
   * TVW applies the 2:4 rule along the compacted K of each packed tile
     (groups of four consecutive kept columns), so L_t % 4 == 0;
   * schedule ("load-balancing through batching"): tiles in order of L_t
-    descending, ties by t ascending; equal L_t form one batch.
+    descending, ties by t ascending; equal L_t form one batch. The table form
+    lists (t, L_t, P_t, Q_t = P_t / 64) per tile in that order.
 
 Layouts (the library's contract, restated):
   R_t = round_up(L_t, 64), P_t = sum_{s<t} R_s.
@@ -24,9 +25,9 @@ Layouts (the library's contract, restated):
       + 64 r + j % 64; zero where j >= L_t or row 128 t + r >= M.
   TVW values: (t, r, c), c < R_t / 2, at 64 P_t + 4096 (c // 32) + 32 r + c % 32.
   TVW meta (canonical): byte b < R_t / 8 of tile row r at 16 P_t + r R_t / 8 + b.
-  TVW meta_hw: tile t owns ceil(R_t / 128) blocks of 128 rows x 16 bytes starting
-      at block Q_t = sum_{s<t} ceil(R_s / 128); row r of block kb holds canonical
-      bytes 16 kb .. 16 kb + 15 of tile row r (0x44 past R_t / 8).
+  TVW meta_hw: tile t owns R_t / 64 blocks of 2048 bytes starting at block
+      Q_t = P_t / 64: the 16-bit operand layout of sp24.meta_hw_from_canonical
+      applied to the tile's canonical metadata (128 rows, K = R_t).
 """
 from __future__ import annotations
 
@@ -74,6 +75,16 @@ def padded(L: np.ndarray) -> np.ndarray:
     return (L + U - 1) // U * U
 
 
+def schedule_table(keep: np.ndarray) -> np.ndarray:
+    """(t, L_t, P_t, Q_t) for the tiles in schedule order, flattened (4 per tile)."""
+    keep = np.asarray(keep, dtype=np.int64)
+    R = padded(keep)
+    P = np.concatenate([[0], np.cumsum(R)])[:-1]
+    Q = P // 64
+    order = schedule(keep)
+    return np.stack([order, keep[order], P[order], Q[order]], axis=1).reshape(-1).astype(np.int32)
+
+
 def gathered_tile(W: np.ndarray, t: int, idx: np.ndarray) -> np.ndarray:
     """The 128 x L_t block W[tile rows][idx] (rows past M are zero)."""
     M, K = W.shape
@@ -97,9 +108,7 @@ def prune(W: np.ndarray, dt: str, keep: np.ndarray, tvw: bool) -> dict:
     idx_all = []
     packed = np.zeros(T * int(P[-1]) // (2 if tvw else 1), dtype=W.dtype)
     meta = np.full(16 * int(P[-1]), 0x44, dtype=np.uint8) if tvw else None
-    nblk = (R + 127) // 128
-    Q = np.concatenate([[0], np.cumsum(nblk)])
-    meta_hw = np.full(2048 * int(Q[-1]), 0x44, dtype=np.uint8) if tvw else None
+    meta_hw = np.zeros(32 * int(P[-1]), dtype=np.uint8) if tvw else None
     for t in range(nt):
         L, Rt, Pt = int(keep[t]), int(R[t]), int(P[t])
         idx = select(s[t], L)
@@ -121,14 +130,12 @@ def prune(W: np.ndarray, dt: str, keep: np.ndarray, tvw: bool) -> dict:
             nbytes = min(m.shape[1], Rt // 8)
             mc[:, :nbytes] = m[:, :nbytes]
             meta[16 * Pt:16 * Pt + T * (Rt // 8)] = mc.reshape(-1)
-            for kb in range(int(nblk[t])):
-                chunk = np.full((T, 16), 0x44, dtype=np.uint8)
-                part = mc[:, 16 * kb:16 * kb + 16]
-                chunk[:, :part.shape[1]] = part
-                b0 = 2048 * (int(Q[t]) + kb)
-                meta_hw[b0:b0 + 2048] = chunk.reshape(-1)
+            if Rt:
+                hw = sp24.meta_hw_from_canonical(mc, T, Rt, dt)
+                meta_hw[32 * Pt:32 * Pt + hw.size] = hw
     indices = np.concatenate(idx_all).astype(np.int32) if idx_all else np.zeros(0, np.int32)
     return {"offsets": offsets_of(keep), "indices": indices, "schedule": schedule(keep),
+            "schedule_table": schedule_table(keep),
             "packed": packed, "meta": meta, "meta_hw": meta_hw, "scores": s}
 
 

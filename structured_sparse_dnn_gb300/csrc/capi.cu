@@ -1,0 +1,305 @@
+// The C ABI: argument validation, host-side tables, and dispatch to the kernels.
+// Every entry point returns an ssdnn_status and never throws.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ssdnn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ssdnn {
+namespace {
+
+// Per-device error word written by kernels whose bounded waits expire.
+__device__ uint32_t g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+
+uint32_t* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int elem_bytes(int dt) { return dt == SSDNN_E4M3 ? 1 : 2; }
+bool valid_dt(int dt) { return dt == SSDNN_F16 || dt == SSDNN_BF16 || dt == SSDNN_E4M3; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? SSDNN_OK : SSDNN_ERR_CUDA; }
+
+// Zero the M x N output (K == 0 or no kept columns anywhere).
+int zero_output(void* Y, int64_t ldy, int64_t M, int64_t N, cudaStream_t s) {
+  if (M == 0 || N == 0) return SSDNN_OK;
+  return from_cuda(cudaMemset2DAsync(Y, static_cast<size_t>(ldy * 2), 0, static_cast<size_t>(N * 2),
+                                     static_cast<size_t>(M), s));
+}
+
+int check_gemm_io(int out_dt, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, int eb, void* Y,
+                  int64_t ldy) {
+  if (out_dt != SSDNN_F16 && out_dt != SSDNN_BF16) return SSDNN_ERR_UNSUPPORTED;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SSDNN_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return SSDNN_OK;
+  if (!Y || (K > 0 && !X)) return SSDNN_ERR_INVALID_ARG;
+  if (ldy < N || (K > 0 && ldx < N)) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (ldy * 2) % 16) return SSDNN_ERR_UNSUPPORTED;
+  if (K > 0 && (!aligned16(X) || (ldx * eb) % 16)) return SSDNN_ERR_UNSUPPORTED;
+  return SSDNN_OK;
+}
+
+struct Tables {
+  TwTables t;
+  std::vector<int32_t> offsets, schedule;
+  int64_t L_total = 0;
+};
+
+int build_tables(int tvw, int64_t M, int64_t K, const int32_t* keep, Tables* out) {
+  const int64_t nt = ceil_div(M, 128);
+  out->t.nt = nt;
+  out->offsets.assign(static_cast<size_t>(nt + 1), 0);
+  std::vector<int64_t> P(static_cast<size_t>(nt), 0), Q(static_cast<size_t>(nt), 0);
+  int64_t p = 0, q = 0, o = 0, maxR = 0;
+  for (int64_t t = 0; t < nt; ++t) {
+    const int64_t L = keep[t];
+    if (L < 0 || L > K) return SSDNN_ERR_INVALID_ARG;
+    if (tvw && (L % 4)) return SSDNN_ERR_UNSUPPORTED;
+    const int64_t R = round_up(L, 64);
+    P[static_cast<size_t>(t)] = p;
+    Q[static_cast<size_t>(t)] = p / 64;  // first 2048-byte metadata block of the tile
+    p += R;
+    q += R / 64;
+    o += L;
+    maxR = std::max(maxR, R);
+    if (o > kMaxDim || 128 * p > kMaxDim) return SSDNN_ERR_UNSUPPORTED;
+    out->offsets[static_cast<size_t>(t + 1)] = static_cast<int32_t>(o);
+  }
+  out->t.P_total = p;
+  out->t.Q_total = q;
+  out->t.max_R = maxR;
+  out->L_total = o;
+  std::vector<int32_t> order(static_cast<size_t>(nt));
+  for (int64_t t = 0; t < nt; ++t) order[static_cast<size_t>(t)] = static_cast<int32_t>(t);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return keep[a] > keep[b]; });
+  out->schedule.resize(static_cast<size_t>(4 * nt));
+  for (int64_t e = 0; e < nt; ++e) {
+    const int32_t t = order[static_cast<size_t>(e)];
+    out->schedule[static_cast<size_t>(4 * e + 0)] = t;
+    out->schedule[static_cast<size_t>(4 * e + 1)] = keep[t];
+    out->schedule[static_cast<size_t>(4 * e + 2)] = static_cast<int32_t>(P[static_cast<size_t>(t)]);
+    out->schedule[static_cast<size_t>(4 * e + 3)] = static_cast<int32_t>(Q[static_cast<size_t>(t)]);
+  }
+  return SSDNN_OK;
+}
+
+}  // namespace
+}  // namespace ssdnn
+
+using namespace ssdnn;
+
+extern "C" {
+
+const char* ssdnn_status_str(int status) {
+  switch (status) {
+    case SSDNN_OK: return "ok";
+    case SSDNN_ERR_INVALID_ARG: return "invalid argument";
+    case SSDNN_ERR_UNSUPPORTED: return "unsupported shape, alignment or dtype";
+    case SSDNN_ERR_CUDA: return "CUDA error";
+    case SSDNN_ERR_TIMEOUT: return "device-side wait timed out";
+    case SSDNN_ERR_DEVICE: return "device error flag set";
+  }
+  return "unknown status";
+}
+
+int ssdnn_version(void) { return 100; }
+
+int ssdnn_check_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSDNN_ERR_CUDA;
+  uint32_t* w = error_word();
+  if (!w) return SSDNN_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SSDNN_ERR_CUDA;
+  if (v) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SSDNN_ERR_CUDA;
+  }
+  if (v & kErrTimeout) return SSDNN_ERR_TIMEOUT;
+  if (v) return SSDNN_ERR_DEVICE;
+  return SSDNN_OK;
+}
+
+int sp24_sizes(int dt, int64_t M, int64_t K, size_t* values_bytes, size_t* meta_bytes, size_t* meta_hw_bytes) {
+  if (!valid_dt(dt) || M < 0 || K < 0 || M > kMaxDim || K > kMaxDim) return SSDNN_ERR_INVALID_ARG;
+  if (K % 4) return SSDNN_ERR_UNSUPPORTED;
+  const int64_t Kp = round_up(K, 32);
+  if (values_bytes) *values_bytes = static_cast<size_t>(M * (Kp / 2) * elem_bytes(dt));
+  if (meta_bytes) *meta_bytes = static_cast<size_t>(M * (Kp / 8));
+  const int64_t span = dt == SSDNN_E4M3 ? 128 : 64;  // K columns per operand metadata block
+  if (meta_hw_bytes) *meta_hw_bytes = static_cast<size_t>(ceil_div(M, 128) * ceil_div(K, span) * 2048);
+  return SSDNN_OK;
+}
+
+int sp24_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, void* values, uint8_t* meta,
+                        uint8_t* meta_hw, void* stream) {
+  if (!valid_dt(dt) || M < 0 || K < 0 || M > kMaxDim || K > kMaxDim) return SSDNN_ERR_INVALID_ARG;
+  if (K % 4) return SSDNN_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return SSDNN_OK;
+  if (!W || !values || !meta_hw || ldw < K) return SSDNN_ERR_INVALID_ARG;
+  const int eb = elem_bytes(dt);
+  if ((reinterpret_cast<uintptr_t>(W) % eb) || !aligned16(values) || !aligned16(meta_hw) ||
+      (meta && (reinterpret_cast<uintptr_t>(meta) & 3u)))
+    return SSDNN_ERR_UNSUPPORTED;
+  return from_cuda(launch_sp24_compress(dt, W, M, K, ldw, values, meta, meta_hw,
+                                        static_cast<cudaStream_t>(stream), error_word()));
+}
+
+int sp24_gemm(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+              const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+              void* stream) {
+  if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
+  const int eb = elem_bytes(in_dt);
+  int st = check_gemm_io(out_dt, M, N, K, X, ldx, eb, Y, ldy);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (K % 4) return SSDNN_ERR_UNSUPPORTED;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(Y, ldy, M, N, s);
+  if (!values || !meta_hw) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(values) || !aligned16(meta_hw)) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = in_dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = values;
+  a.lda = round_up(K, 32) / 2;
+  a.meta_hw = meta_hw;
+  a.X = X;
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  return from_cuda(launch_gemm(1, a, s, error_word()));
+}
+
+int dense_gemm(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
+               const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, void* stream) {
+  if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
+  const int eb = elem_bytes(in_dt);
+  int st = check_gemm_io(out_dt, M, N, K, X, ldx, eb, Y, ldy);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(Y, ldy, M, N, s);
+  if (!W || ldw < K) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(W) || (ldw * eb) % 16) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = in_dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = W;
+  a.lda = ldw;
+  a.X = X;
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  return from_cuda(launch_gemm(0, a, s, error_word()));
+}
+
+int tw_sizes(int dt, int tvw, int64_t M, int64_t K, const int32_t* keep_counts_host, size_t* packed_bytes,
+             size_t* indices_count, size_t* meta_bytes, size_t* meta_hw_bytes, size_t* workspace_bytes) {
+  if ((dt != SSDNN_F16 && dt != SSDNN_BF16) || M < 0 || K < 0 || M > kMaxDim || K > kMaxDim)
+    return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  if (M > 0 && !keep_counts_host) return SSDNN_ERR_INVALID_ARG;
+  Tables tb;
+  int st = build_tables(tvw, M, K, keep_counts_host, &tb);
+  if (st != SSDNN_OK) return st;
+  const int64_t P = tb.t.P_total;
+  if (packed_bytes) *packed_bytes = static_cast<size_t>((tvw ? 64 : 128) * P * 2);
+  if (indices_count) *indices_count = static_cast<size_t>(tb.L_total);
+  if (meta_bytes) *meta_bytes = tvw ? static_cast<size_t>(16 * P) : 0;
+  if (meta_hw_bytes) *meta_hw_bytes = tvw ? static_cast<size_t>(2048 * tb.t.Q_total) : 0;
+  if (workspace_bytes) *workspace_bytes = static_cast<size_t>(tb.t.nt * K * 4);
+  return SSDNN_OK;
+}
+
+int tw_prune_compress(int dt, int tvw, const void* W, int64_t M, int64_t K, int64_t ldw,
+                      const int32_t* keep_counts_host, int32_t* offsets, int32_t* indices, int32_t* schedule,
+                      void* packed, uint8_t* meta, uint8_t* meta_hw, void* workspace, void* stream) {
+  if ((dt != SSDNN_F16 && dt != SSDNN_BF16) || M < 0 || K < 0 || M > kMaxDim || K > kMaxDim)
+    return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  if (M == 0) return SSDNN_OK;
+  if (!keep_counts_host || !offsets || !schedule) return SSDNN_ERR_INVALID_ARG;
+  Tables tb;
+  int st = build_tables(tvw, M, K, keep_counts_host, &tb);
+  if (st != SSDNN_OK) return st;
+  if (K > 0 && (!W || ldw < K || !workspace)) return SSDNN_ERR_INVALID_ARG;
+  if (tb.L_total > 0 && !indices) return SSDNN_ERR_INVALID_ARG;
+  if (tb.t.P_total > 0 && (!packed || (tvw && (!meta || !meta_hw)))) return SSDNN_ERR_INVALID_ARG;
+  if ((W && (reinterpret_cast<uintptr_t>(W) & 1u)) || (packed && !aligned16(packed)) ||
+      (meta && !aligned16(meta)) || (meta_hw && !aligned16(meta_hw)) || (workspace && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(offsets) & 3u) || (reinterpret_cast<uintptr_t>(schedule) & 3u) ||
+      (indices && (reinterpret_cast<uintptr_t>(indices) & 3u)))
+    return SSDNN_ERR_UNSUPPORTED;
+  auto s = static_cast<cudaStream_t>(stream);
+  // Host tables (pageable source: the copy is staged before the call returns).
+  cudaError_t e = cudaMemcpyAsync(offsets, tb.offsets.data(), tb.offsets.size() * sizeof(int32_t),
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(schedule, tb.schedule.data(), tb.schedule.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return SSDNN_ERR_CUDA;
+  return from_cuda(launch_tw_prune(dt, tvw, W, M, K, ldw, tb.t, offsets, indices, schedule, packed, meta, meta_hw,
+                                   static_cast<float*>(workspace), s, error_word()));
+}
+
+int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* keep_counts_host,
+             const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+             const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream) {
+  if (dt != SSDNN_F16 && dt != SSDNN_BF16) return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  int st = check_gemm_io(dt, M, N, K, X, ldx, 2, Y, ldy);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (!keep_counts_host) return SSDNN_ERR_INVALID_ARG;
+  Tables tb;
+  st = build_tables(tvw, M, K, keep_counts_host, &tb);
+  if (st != SSDNN_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0 || tb.t.P_total == 0) return zero_output(Y, ldy, M, N, s);
+  if (!offsets || !indices || !schedule || !packed || (tvw && !meta_hw)) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(packed) || (tvw && !aligned16(meta_hw))) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = dt;
+  a.out_dt = dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = packed;
+  a.meta_hw = meta_hw;
+  a.X = X;
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = 1.0f;
+  a.nt = tb.t.nt;
+  a.packed_rows = 2 * tb.t.P_total;
+  a.offsets = offsets;
+  a.indices = indices;
+  a.schedule = schedule;
+  return from_cuda(launch_gemm(tvw ? 3 : 2, a, s, error_word()));
+}
+
+}  // extern "C"

@@ -1,0 +1,496 @@
+// The tensor-core GEMM family: dense, 2:4 sparse, tile-wise (TW) and
+// tile-vector-wise (TVW), one persistent warp-specialised kernel template.
+//
+// Y = alpha * A . X with A the weight operand (M x K, K-major) and X the
+// activations (K x N, N contiguous, i.e. an MN-major B operand).
+//   dense : A = W.
+//   sp24  : A = the 2:4-compressed values (K/2 wide) and its position metadata;
+//           the sparse tensor core skips the zero half ("Accelerating Sparse Deep
+//           Neural Networks", Abstract: twice the math rate of dense units).
+//   TW    : per 128-row tile, A = the packed kept columns and the B rows are
+//           gathered from X by the tile's index list -- the tile-wise pattern is
+//           applied where operands come from global memory ("Accelerating Sparse
+//           DNNs Based on Tiled GEMM", Abstract).
+//   TVW   : TW with the packed tile in 2:4 form, executed on the sparse tensor
+//           core (same page: 2:4 inside the tensor core, TW at global memory).
+// Tiles are handed out in the schedule order (longest kept length first, equal
+// lengths adjacent: "load-balancing through batching", same page, TL;DR), and the
+// gather, MMA and epilogue run fused in one kernel ("kernel fusion", same TL;DR).
+//
+// Roles (256 threads, one CTA per SM, persistent over work units):
+//   warp 0      producer: TMA tiles of A and B (B by 4-row gathers for TW/TVW),
+//               1-D bulk copy of the 2:4 metadata blocks, into a ring of stages.
+//   warp 1      MMA issuer: tcgen05.cp of metadata to TMEM, tcgen05.mma(.sp) into
+//               a TMEM fp32 accumulator, commits release stages / publish tiles.
+//   warp 2      TMEM allocator.
+//   warps 4..7  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//               32 (w % 4) ..), scale by alpha, round to the output type, store.
+//
+// Stage geometry (bytes are the same for 16-bit and 8-bit inputs):
+//   BK = 128 / elem_bytes dense K per stage (64 fp16/bf16, 128 e4m3).
+//   A  : 128 rows x 128 B (dense, 128B swizzle) or 128 rows x 64 B (sparse
+//        values, 64B swizzle).
+//   B  : BK rows x BN columns, as BN*eb/128 boxes of BK rows x 128 B, 128B swizzle
+//        (MN-major canonical layout: 8-row atoms of 1024 B, boxes BK*128 B apart).
+//   meta (sparse): one 2048-byte block per stage = 128 rows x 16 B, copied to
+//        four TMEM columns; instruction j reads its metadata at column 2 j.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ssdnn {
+namespace {
+
+struct Params {
+  int32_t M, N;
+  int32_t MB, NB;           // 128-row blocks, BN-column blocks
+  int32_t num_units;
+  int32_t nk;               // k stages per unit (dense / sp24)
+  int32_t out_dt;           // 0 f16, 1 bf16
+  float alpha;
+  const uint8_t* meta_hw;
+  const int32_t* schedule;  // TW/TVW: (t, L, P, Q) per tile, in work order
+  const int32_t* offsets;
+  const int32_t* indices;
+  uint8_t* Y;
+  int64_t ldy;              // elements
+  uint32_t* err;
+};
+
+template <int DT, bool SPARSE, bool GATHER, int BN>
+struct Cfg {
+  static constexpr int EB = Elem<DT>::bytes;
+  static constexpr bool F8 = Elem<DT>::f8;
+  static constexpr int BK = 128 / EB;                       // dense K per stage
+  static constexpr int A_BYTES = SPARSE ? 128 * 64 : 128 * 128;
+  static constexpr int B_BYTES = 128 * BN;                  // BK * BN * EB
+  static constexpr int META_BYTES = SPARSE ? 2048 : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + META_BYTES;
+  static constexpr int STAGES_RAW = (220 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int MMA_K = (SPARSE ? 64 : 32) / EB;      // dense K per instruction
+  static constexpr int MMAS = BK / MMA_K;                    // instructions per stage
+  static constexpr int B_BOX_COLS = 128 / EB;                // columns per 128-byte B box
+  static constexpr int B_BOXES = BN / B_BOX_COLS;
+  static constexpr int B_BOX_BYTES = BK * 128;
+  static constexpr int NACC = (BN >= 256) ? 1 : 2;
+  static constexpr int META_COL0 = 256;                      // TMEM columns 256.. hold metadata
+  static constexpr int META_SLOTS = 4;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t IDESC = ptx::idesc(Elem<DT>::mma_fmt, Elem<DT>::mma_fmt, SPARSE, 128, BN,
+                                               false, true);
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(B_BOXES * B_BOX_COLS == BN, "BN must be a multiple of the 128-byte box width");
+  static_assert(NACC * BN <= META_COL0, "accumulators overlap the metadata columns");
+};
+
+struct UnitInfo {
+  int32_t m0, n0, nk;
+  int32_t a_row0;     // packed-operand row of the first chunk (TW/TVW)
+  int32_t meta_blk0;  // first metadata block index
+  int32_t idx_base;   // offsets[t] (TW/TVW)
+  int32_t L;          // kept count (TW/TVW)
+};
+
+template <typename C, bool GATHER>
+__device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u) {
+  UnitInfo ui;
+  if constexpr (!GATHER) {
+    const int32_t mb = u % p.MB, nb = u / p.MB;
+    ui.m0 = mb * 128;
+    ui.n0 = nb * (C::B_BOXES * C::B_BOX_COLS);
+    ui.nk = p.nk;
+    ui.a_row0 = ui.m0;
+    ui.meta_blk0 = mb * p.nk;  // one 2048-byte metadata block per stage
+    ui.idx_base = 0;
+    ui.L = 0;
+  } else {
+    const int32_t e = u / p.NB, nb = u % p.NB;
+    const int32_t* s = p.schedule + 4 * e;
+    const int32_t t = __ldg(s + 0), L = __ldg(s + 1), P = __ldg(s + 2), Q = __ldg(s + 3);
+    ui.m0 = t * 128;
+    ui.n0 = nb * (C::B_BOXES * C::B_BOX_COLS);
+    ui.nk = (L + C::BK - 1) / C::BK;
+    ui.a_row0 = 2 * P;  // packed chunks: 128 rows each, tile t starts at row 2 P
+    ui.meta_blk0 = Q;
+    ui.idx_base = __ldg(p.offsets + t);
+    ui.L = L;
+  }
+  return ui;
+}
+
+template <int DT, bool SPARSE, bool GATHER, int BN>
+__global__ void __launch_bounds__(256, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using C = Cfg<DT, SPARSE, GATHER, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* acc_full = bars + 2 * C::STAGES;
+  uint64_t* acc_empty = acc_full + C::NACC;
+  uint64_t* drain = acc_empty + C::NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::NACC; ++a) {
+      ptx::mbar_init(&acc_full[a], 1);
+      ptx::mbar_init(&acc_empty[a], 128);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_a = ptx::policy_evict_last();
+    const uint64_t pol_b = ptx::policy_evict_normal();
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int32_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const UnitInfo ui = decode_unit<C, GATHER>(p, u);
+      for (int32_t kb = 0; kb < ui.nk; ++kb) {
+        if (*abort_flag) { ok = false; break; }
+        if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, p.err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) { *abort_flag = 1; break; }
+        uint8_t* sA = smem + stage * C::STAGE_BYTES;
+        uint8_t* sB = sA + C::A_BYTES;
+        uint8_t* sM = sB + C::B_BYTES;
+        constexpr bool meta_now = SPARSE;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&full[stage],
+                                     C::A_BYTES + C::B_BYTES + (meta_now ? C::META_BYTES : 0));
+          // A: dense W / 2:4 values box (inner coordinate in elements)
+          const int32_t a_col = GATHER ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
+          const int32_t a_row = GATHER ? ui.a_row0 + 128 * kb : ui.m0;
+          ptx::tma_load_2d(sA, &tmA, &full[stage], a_col, a_row, pol_a);
+          if (meta_now) {
+            const uint8_t* src = p.meta_hw + static_cast<int64_t>(ui.meta_blk0 + kb) * 2048;
+            ptx::bulk_load(sM, src, 2048, &full[stage], pol_a);
+          }
+          if constexpr (!GATHER) {
+#pragma unroll
+            for (int bx = 0; bx < C::B_BOXES; ++bx)
+              ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS,
+                               kb * C::BK, pol_b);
+          }
+        }
+        if constexpr (GATHER) {
+          __syncwarp();
+          // lanes 0..15 gather four X rows each (positions past L read row 0; the
+          // packed A is zero there)
+          if (lane < C::BK / 4) {
+            int32_t rr[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int32_t j = kb * C::BK + 4 * static_cast<int32_t>(lane) + q;
+              rr[q] = (j < ui.L) ? __ldg(p.indices + ui.idx_base + j) : 0;
+            }
+#pragma unroll
+            for (int bx = 0; bx < C::B_BOXES; ++bx)
+              ptx::tma_gather4(sB + bx * C::B_BOX_BYTES + 4 * lane * 128, &tmB, &full[stage],
+                               ui.n0 + bx * C::B_BOX_COLS, rr[0], rr[1], rr[2], rr[3], pol_b);
+          }
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    // On abort, wait (bounded) for the copies still in flight before exiting.
+    if (!ok && lane == 0) {
+      int s = stage;
+      uint32_t ph = phase;
+      const int pending = issued < C::STAGES ? issued : C::STAGES;
+      for (int n = 0; n < pending; ++n) {
+        if (--s < 0) { s = C::STAGES - 1; ph ^= 1u; }
+        wait_bounded(&full[s], ph, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int meta_slot = 0;
+    bool ok = true;
+    for (int32_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const UnitInfo ui = decode_unit<C, GATHER>(p, u);
+      if (lane == 0) ok = wait_bounded(&acc_empty[acc], acc_phase ^ 1u, p.err);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || *abort_flag) { *abort_flag = 1; ok = false; break; }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      uint32_t cur_meta = 0;
+      for (int32_t kb = 0; kb < ui.nk; ++kb) {
+        if (lane == 0) ok = wait_bounded(&full[stage], phase, p.err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) { *abort_flag = 1; break; }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sA = ptx::smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sB = sA + C::A_BYTES;
+          if constexpr (SPARSE) {
+            const uint32_t sM = sB + C::B_BYTES;
+            cur_meta = tmem_base + C::META_COL0 + 4u * static_cast<uint32_t>(meta_slot);
+            meta_slot = (meta_slot + 1) % C::META_SLOTS;
+            // 128 rows x 16 B, rows contiguous: 8-row core matrices 128 B apart
+            ptx::tmem_cp_128x128b(cur_meta, ptx::sdesc(sM, 128, 128, 0));
+          }
+#pragma unroll
+          for (int j = 0; j < C::MMAS; ++j) {
+            const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+            const uint64_t bdesc = ptx::sdesc(sB + j * C::MMA_K * 128, C::B_BOX_BYTES, 1024, 2);
+            if constexpr (SPARSE) {
+              const uint64_t adesc = ptx::sdesc(sA + j * 32, 16, 512, 4);
+              // the metadata of instruction j starts at column 2 j of the stage's four
+              // (the sparse MMA reads it from an even column: one column for a
+              // 16-bit K = 32 step, two for an e4m3 K = 64 step)
+              const uint32_t col = 2u * j;
+              if constexpr (C::F8)
+                ptx::mma_sp_f8(d_tmem, adesc, bdesc, cur_meta + col, C::IDESC, accum);
+              else
+                ptx::mma_sp_f16(d_tmem, adesc, bdesc, cur_meta + col, C::IDESC, accum);
+            } else {
+              const uint64_t adesc = ptx::sdesc(sA + j * 32, 16, 1024, 2);
+              if constexpr (C::F8)
+                ptx::mma_f8(d_tmem, adesc, bdesc, C::IDESC, accum);
+              else
+                ptx::mma_f16(d_tmem, adesc, bdesc, C::IDESC, accum);
+            }
+          }
+          ptx::mma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::mma_commit(&acc_full[acc]);
+      __syncwarp();
+      if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+    }
+    // Make sure no MMA is still writing TMEM when the allocation is released.
+    if (lane == 0) {
+      ptx::mma_commit(drain);
+      wait_bounded(drain, 0, nullptr);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t q = warp & 3u;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int32_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const UnitInfo ui = decode_unit<C, GATHER>(p, u);
+      ok = wait_bounded(&acc_full[acc], acc_phase, p.err);
+      if (!ok || *abort_flag) { *abort_flag = 1; break; }
+      ptx::tc_fence_after();
+      const int32_t row = ui.m0 + static_cast<int32_t>(32 * q + lane);
+      const bool row_ok = row < p.M;
+      uint8_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy * 2;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        if (ui.nk > 0) {
+          ptx::tmem_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(acc * BN + 32 * c), r);
+          ptx::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (c == BN / 32 - 1) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&acc_empty[acc]);
+        }
+        const int32_t n0 = ui.n0 + 32 * c;
+        if (!row_ok || n0 >= p.N) continue;
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = __uint_as_float(r[2 * i]) * p.alpha;
+          const float x1 = __uint_as_float(r[2 * i + 1]) * p.alpha;
+          if (p.out_dt == 1) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+            packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+          } else {
+            const __half2 h = __floats2half2_rn(x0, x1);
+            packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+        }
+        uint16_t* dst = reinterpret_cast<uint16_t*>(yrow) + n0;
+        if (n0 + 32 <= p.N) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            reinterpret_cast<uint4*>(dst)[v] =
+                make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (n0 + i < p.N) dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
+        }
+      }
+      if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D tensor map over a row-major matrix (rows x cols elements, pitch in bytes).
+bool make_map(CUtensorMap* m, const void* base, int eb, uint64_t cols, uint64_t rows, uint64_t pitch_bytes,
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                        const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int DT, bool SPARSE, bool GATHER, int BN>
+cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
+  using C = Cfg<DT, SPARSE, GATHER, BN>;
+  const int eb = C::EB;
+  CUtensorMap tA, tB;
+  bool ok;
+  if constexpr (!GATHER) {
+    if constexpr (SPARSE)
+      ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, 128,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+    else
+      ok = make_map(&tA, a.A, eb, a.K, a.M, a.lda * eb, 128 / eb, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, 128 / eb, C::BK, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    // packed operand seen as (packed_rows x 64) dense or (packed_rows x 32) values
+    if constexpr (SPARSE)
+      ok = make_map(&tA, a.A, eb, 32, a.packed_rows, 64, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+    else
+      ok = make_map(&tA, a.A, eb, 64, a.packed_rows, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, 128 / eb, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+
+  Params p{};
+  p.M = static_cast<int32_t>(a.M);
+  p.N = static_cast<int32_t>(a.N);
+  p.MB = static_cast<int32_t>(ceil_div(a.M, 128));
+  p.NB = static_cast<int32_t>(ceil_div(a.N, BN));
+  p.nk = static_cast<int32_t>(ceil_div(a.K, C::BK));
+  p.num_units = GATHER ? static_cast<int32_t>(a.nt) * p.NB : p.MB * p.NB;
+  p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : 0;
+  p.alpha = a.alpha;
+  p.meta_hw = a.meta_hw;
+  p.schedule = a.schedule;
+  p.offsets = a.offsets;
+  p.indices = a.indices;
+  p.Y = static_cast<uint8_t*>(a.Y);
+  p.ldy = a.ldy;
+  p.err = err;
+  if (p.num_units == 0) return cudaSuccess;
+
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = std::min(p.num_units, sm_count());
+  kern<<<grid, 256, C::SMEM_BYTES, s>>>(tA, tB, p);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err) {
+  // Narrow N or few 128-row blocks: a 128-wide N tile gives more work units.
+  const int64_t units256 = ceil_div(a.M, 128) * ceil_div(a.N, 256);
+  const bool narrow = (a.N <= 128) || (mode < 2 && units256 < 2 * sm_count());
+  switch (mode) {
+    case 0:
+      return narrow ? run<DT, false, false, 128>(a, s, err) : run<DT, false, false, 256>(a, s, err);
+    case 1:
+      return narrow ? run<DT, true, false, 128>(a, s, err) : run<DT, true, false, 256>(a, s, err);
+    case 2:
+      if constexpr (DT != 2) return narrow ? run<DT, false, true, 128>(a, s, err) : run<DT, false, true, 256>(a, s, err);
+      break;
+    case 3:
+      if constexpr (DT != 2) return narrow ? run<DT, true, true, 128>(a, s, err) : run<DT, true, true, 256>(a, s, err);
+      break;
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err) {
+  switch (a.dt) {
+    case SSDNN_F16: return dispatch_dt<0>(mode, a, s, err);
+    case SSDNN_BF16: return dispatch_dt<1>(mode, a, s, err);
+    case SSDNN_E4M3: return dispatch_dt<2>(mode, a, s, err);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ssdnn

@@ -1,0 +1,47 @@
+// Host-side launchers of the kernels; called by the C ABI after validation.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ssdnn {
+
+// 2:4 magnitude prune + compress (one streaming pass over W).
+cudaError_t launch_sp24_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, void* values,
+                                 uint8_t* meta, uint8_t* meta_hw, cudaStream_t s, uint32_t* err);
+
+struct GemmArgs {
+  int dt, out_dt;
+  int64_t M, N, K;
+  const void* A;         // dense W, 2:4 values, or TW/TVW packed operand
+  int64_t lda;           // elements (dense W pitch or values pitch)
+  const uint8_t* meta_hw;
+  const void* X;
+  int64_t ldx;
+  void* Y;
+  int64_t ldy;
+  float alpha;
+  // tile-wise only
+  int64_t nt;            // number of 128-row tiles
+  int64_t packed_rows;   // rows of the packed operand seen as a (rows x 64 or 32) matrix
+  const int32_t* offsets;
+  const int32_t* indices;
+  const int32_t* schedule;
+};
+
+// mode: 0 dense, 1 sp24, 2 TW (dense packed + gather), 3 TVW (2:4 packed + gather)
+cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err);
+
+// Tile-wise prune: scores -> per-tile top-L selection -> pack (TVW: + 2:4).
+struct TwTables {
+  int64_t nt;
+  int64_t P_total;  // sum of round_up(L_t, 64)
+  int64_t Q_total;  // metadata blocks: sum of R_t / 64
+  int64_t max_R;    // max R_t
+};
+cudaError_t launch_tw_prune(int dt, int tvw, const void* W, int64_t M, int64_t K, int64_t ldw,
+                            const TwTables& tabs, const int32_t* offsets, int32_t* indices,
+                            const int32_t* schedule, void* packed, uint8_t* meta, uint8_t* meta_hw,
+                            float* scores, cudaStream_t s, uint32_t* err);
+
+}  // namespace ssdnn

@@ -1,0 +1,196 @@
+"""Thin ctypes binding of libssdnn.so (include/ssdnn.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. Functions carry the C names; the tensor-level helpers allocate the
+outputs with torch (the library itself allocates nothing) and pass raw device
+pointers plus the current CUDA stream. There is no CPU fallback: importing this
+module raises if the library cannot be loaded.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libssdnn.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libssdnn.so not built ({_LIB_PATH}); run structured_sparse_dnn_gb300.build.build()")
+lib = C.CDLL(_LIB_PATH)
+
+F16, BF16, E4M3 = 0, 1, 2
+_DT = {torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3}
+_TORCH = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.float8_e4m3fn}
+
+_i64, _ptr, _sz, _i32p = C.c_int64, C.c_void_p, C.c_size_t, C.POINTER(C.c_int32)
+_SIGS = {
+    "ssdnn_status_str": ([C.c_int], C.c_char_p),
+    "ssdnn_version": ([], C.c_int),
+    "ssdnn_check_device_error": ([_ptr], C.c_int),
+    "sp24_sizes": ([C.c_int, _i64, _i64, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
+    "sp24_prune_compress": ([C.c_int, _ptr, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], C.c_int),
+    "sp24_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _i64, _ptr, _i64, C.c_float, _ptr],
+                  C.c_int),
+    "dense_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, C.c_float, _ptr],
+                   C.c_int),
+    "tw_sizes": ([C.c_int, C.c_int, _i64, _i64, _i32p, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz),
+                  C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
+    "tw_prune_compress": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                           _ptr, _ptr], C.c_int),
+    "tvw_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _ptr,
+                  _i64, _ptr], C.c_int),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+class SsdnnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {lib.ssdnn_status_str(status).decode()} (status {status})")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise SsdnnError(status, where)
+
+
+def _stream(dev) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _keep_arr(keep) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(keep, dtype=np.int32))
+
+
+def _kp(keep: np.ndarray):
+    return keep.ctypes.data_as(_i32p)
+
+
+def status_str(status: int) -> str:
+    return lib.ssdnn_status_str(status).decode()
+
+
+def check_device_error(stream: int | None = None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return lib.ssdnn_check_device_error(stream if stream is not None else _stream(None))
+
+
+# ---------------------------------------------------------------------- 2:4
+def sp24_sizes(dt: int, M: int, K: int) -> tuple[int, int, int]:
+    v, m, h = _sz(), _sz(), _sz()
+    _check(lib.sp24_sizes(dt, M, K, C.byref(v), C.byref(m), C.byref(h)), "sp24_sizes")
+    return v.value, m.value, h.value
+
+
+def sp24_prune_compress(W: torch.Tensor, canonical_meta: bool = True):
+    """W (M x K, fp16/bf16/e4m3, CUDA) -> (values M x Kp/2, meta M x Kp/8 or None, meta_hw bytes)."""
+    dt = _DT[W.dtype]
+    M, K = W.shape
+    assert W.stride(1) == 1
+    vb, mb, hb = sp24_sizes(dt, M, K)
+    Kp = (K + 31) // 32 * 32
+    values = torch.empty((M, Kp // 2), dtype=W.dtype, device=W.device)
+    meta = torch.empty((M, Kp // 8), dtype=torch.uint8, device=W.device) if canonical_meta else None
+    meta_hw = torch.empty(hb, dtype=torch.uint8, device=W.device)
+    _check(lib.sp24_prune_compress(dt, _p(W), M, K, W.stride(0), _p(values), _p(meta), _p(meta_hw),
+                                   _stream(W.device)), "sp24_prune_compress")
+    return values, meta, meta_hw
+
+
+def sp24_gemm(values: torch.Tensor, meta_hw: torch.Tensor, X: torch.Tensor, K: int,
+              out_dtype: torch.dtype | None = None, alpha: float = 1.0, out: torch.Tensor | None = None):
+    """Y = alpha * decompress(values, meta_hw) . X  (M x N)."""
+    dt = _DT[X.dtype]
+    M = values.shape[0]
+    N = X.shape[1]
+    out_dtype = out_dtype or (torch.bfloat16 if dt == E4M3 else X.dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=X.device)
+    _check(lib.sp24_gemm(dt, _DT[out.dtype], M, N, K, _p(values), _p(meta_hw), _p(X), X.stride(0), _p(out),
+                         out.stride(0), alpha, _stream(X.device)), "sp24_gemm")
+    return out
+
+
+def dense_gemm(W: torch.Tensor, X: torch.Tensor, out_dtype: torch.dtype | None = None, alpha: float = 1.0,
+               out: torch.Tensor | None = None):
+    dt = _DT[W.dtype]
+    M, K = W.shape
+    N = X.shape[1]
+    out_dtype = out_dtype or (torch.bfloat16 if dt == E4M3 else W.dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=X.device)
+    _check(lib.dense_gemm(dt, _DT[out.dtype], M, N, K, _p(W), W.stride(0), _p(X), X.stride(0), _p(out),
+                          out.stride(0), alpha, _stream(X.device)), "dense_gemm")
+    return out
+
+
+# ---------------------------------------------------------------- TW / TVW
+@dataclass
+class TileWise:
+    """A tile-wise (or tile-vector-wise) compressed weight, as laid out on the device."""
+    dt: int
+    tvw: bool
+    M: int
+    K: int
+    keep: np.ndarray
+    offsets: torch.Tensor
+    indices: torch.Tensor
+    schedule: torch.Tensor
+    packed: torch.Tensor
+    meta: torch.Tensor | None
+    meta_hw: torch.Tensor | None
+
+
+def tw_sizes(dt: int, tvw: bool, M: int, K: int, keep) -> dict:
+    k = _keep_arr(keep)
+    out = [_sz() for _ in range(5)]
+    _check(lib.tw_sizes(dt, int(tvw), M, K, _kp(k), *[C.byref(o) for o in out]), "tw_sizes")
+    return dict(zip(("packed_bytes", "indices_count", "meta_bytes", "meta_hw_bytes", "workspace_bytes"),
+                    (o.value for o in out)))
+
+
+def tw_prune_compress(W: torch.Tensor, keep, tvw: bool, workspace: torch.Tensor | None = None) -> TileWise:
+    dt = _DT[W.dtype]
+    M, K = W.shape
+    assert W.stride(1) == 1
+    k = _keep_arr(keep)
+    sz = tw_sizes(dt, tvw, M, K, k)
+    dev = W.device
+    nt = (M + 127) // 128
+    offsets = torch.empty(nt + 1, dtype=torch.int32, device=dev)
+    indices = torch.empty(max(1, sz["indices_count"]), dtype=torch.int32, device=dev)
+    schedule = torch.empty(4 * max(1, nt), dtype=torch.int32, device=dev)
+    packed = torch.empty(max(8, sz["packed_bytes"] // 2), dtype=W.dtype, device=dev)
+    meta = torch.empty(max(16, sz["meta_bytes"]), dtype=torch.uint8, device=dev) if tvw else None
+    meta_hw = torch.empty(max(16, sz["meta_hw_bytes"]), dtype=torch.uint8, device=dev) if tvw else None
+    if workspace is None:
+        workspace = torch.empty(max(16, sz["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    _check(lib.tw_prune_compress(dt, int(tvw), _p(W), M, K, W.stride(0), _kp(k), _p(offsets), _p(indices),
+                                 _p(schedule), _p(packed), _p(meta), _p(meta_hw), _p(workspace), _stream(dev)),
+           "tw_prune_compress")
+    return TileWise(dt, tvw, M, K, k, offsets, indices[:sz["indices_count"]], schedule[:4 * nt],
+                    packed[:sz["packed_bytes"] // 2],
+                    None if meta is None else meta[:sz["meta_bytes"]],
+                    None if meta_hw is None else meta_hw[:sz["meta_hw_bytes"]])
+
+
+def tvw_gemm(form: TileWise, X: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    N = X.shape[1]
+    if out is None:
+        out = torch.empty((form.M, N), dtype=X.dtype, device=X.device)
+    _check(lib.tvw_gemm(form.dt, int(form.tvw), form.M, N, form.K, _kp(form.keep), _p(form.offsets),
+                        _p(form.indices), _p(form.schedule), _p(form.packed), _p(form.meta_hw), _p(X),
+                        X.stride(0), _p(out), out.stride(0), _stream(X.device)), "tvw_gemm")
+    return out

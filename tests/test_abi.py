@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports every function include/ssdnn.h
+declares; host-only entry points (sizes, status strings, argument checks that
+fail before any CUDA call) behave as documented. No GPU needed."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssdnn.h")
+
+
+@pytest.fixture(scope="module")
+def ssdnn():
+    from structured_sparse_dnn_gb300 import build
+    build.build()
+    from structured_sparse_dnn_gb300 import ssdnn as mod
+    return mod
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    for n in ("sp24_prune_compress", "sp24_gemm", "tw_prune_compress", "tvw_gemm", "dense_gemm",
+              "sp24_sizes", "tw_sizes", "ssdnn_status_str", "ssdnn_check_device_error", "ssdnn_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(ssdnn):
+    lib = C.CDLL(os.path.join(ROOT, "structured_sparse_dnn_gb300", "lib", "libssdnn.so"))
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert set(ssdnn.EXPORTED) <= set(_declared())
+
+
+def test_status_strings_and_version(ssdnn):
+    assert ssdnn.status_str(0) == "ok"
+    assert "unsupported" in ssdnn.status_str(2)
+    assert ssdnn.status_str(99) == "unknown status"
+    assert ssdnn.lib.ssdnn_version() >= 100
+
+
+def test_sp24_sizes(ssdnn):
+    assert ssdnn.sp24_sizes(ssdnn.BF16, 256, 256) == (256 * 128 * 2, 256 * 32, 2 * 4 * 2048)
+    assert ssdnn.sp24_sizes(ssdnn.E4M3, 14336, 4096) == (14336 * 2048, 14336 * 512, 112 * 32 * 2048)
+    v, m, h = ssdnn.sp24_sizes(ssdnn.F16, 5, 36)           # Kp = 64
+    assert (v, m, h) == (5 * 32 * 2, 5 * 8, 1 * 1 * 2048)
+    with pytest.raises(ssdnn.SsdnnError) as e:
+        ssdnn.sp24_sizes(ssdnn.F16, 4, 6)
+    assert e.value.status == 2
+    with pytest.raises(ssdnn.SsdnnError) as e:
+        ssdnn.sp24_sizes(7, 4, 8)
+    assert e.value.status == 1
+
+
+def test_tw_sizes_match_layout(ssdnn):
+    keep = np.array([832, 0, 64, 100], dtype=np.int32)
+    s = ssdnn.tw_sizes(ssdnn.BF16, False, 500, 1024, keep)
+    R = [832, 0, 64, 128]
+    assert s["packed_bytes"] == 128 * sum(R) * 2
+    assert s["indices_count"] == keep.sum()
+    assert s["workspace_bytes"] == 4 * 1024 * 4
+    assert s["meta_bytes"] == 0 and s["meta_hw_bytes"] == 0
+    with pytest.raises(ssdnn.SsdnnError):                    # TVW needs L % 4 == 0
+        ssdnn.tw_sizes(ssdnn.BF16, True, 500, 1024, np.array([832, 0, 64, 102], dtype=np.int32))
+    keep4 = np.array([832, 0, 64, 100], dtype=np.int32)
+    s = ssdnn.tw_sizes(ssdnn.BF16, True, 500, 1024, keep4)
+    assert s["packed_bytes"] == 64 * sum(R) * 2
+    assert s["meta_bytes"] == 16 * sum(R)
+    assert s["meta_hw_bytes"] == 2048 * (13 + 0 + 1 + 2)
+    with pytest.raises(ssdnn.SsdnnError):                    # L > K
+        ssdnn.tw_sizes(ssdnn.BF16, False, 128, 64, np.array([65], dtype=np.int32))
+    with pytest.raises(ssdnn.SsdnnError) as e:               # e4m3 tile-wise is not implemented
+        ssdnn.tw_sizes(ssdnn.E4M3, False, 128, 64, np.array([64], dtype=np.int32))
+    assert e.value.status == 2
+
+
+def test_argument_errors_before_any_device_work(ssdnn):
+    lib = ssdnn.lib
+    # bad dtype, negative sizes, K % 4 != 0: rejected on the host
+    assert lib.sp24_prune_compress(9, None, 4, 8, 8, None, None, None, None) == 1
+    assert lib.sp24_prune_compress(0, None, -1, 8, 8, None, None, None, None) == 1
+    assert lib.sp24_prune_compress(0, None, 4, 6, 6, None, None, None, None) == 2
+    assert lib.sp24_gemm(0, 2, 4, 4, 8, None, None, None, 4, None, 4, 1.0, None) == 2   # out e4m3
+    assert lib.sp24_gemm(0, 0, 4, 4, 8, None, None, None, 4, None, 4, 1.0, None) == 1   # null Y
+    assert lib.dense_gemm(0, 0, 4, 8, 8, 16, 8, 16, 4, 32, 8, 1.0, None) == 1           # ldx < N
+    assert lib.tvw_gemm(2, 0, 4, 4, 8, None, None, None, None, None, None, None, 4, None, 4, None) == 2
+    # empty problems are valid no-ops
+    assert lib.sp24_gemm(0, 0, 0, 4, 8, None, None, None, 4, None, 4, 1.0, None) == 0
+    assert lib.sp24_prune_compress(0, None, 0, 8, 8, None, None, None, None) == 0

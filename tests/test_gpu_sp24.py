@@ -1,0 +1,145 @@
+"""GPU parity of the 2:4 path through the C ABI: prune/compress bit-exact
+against the oracle, sparse and dense GEMMs within the elementwise bound,
+ragged shapes, edge values, strided operands and untouched canaries."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (REL, bits_of, canary_intact, dev_padded, dev_tensor, guarded_output, lib,
+                         rand_bits)
+
+pytestmark = pytest.mark.gpu
+
+SHAPES_C = [(1, 4), (5, 36), (128, 128), (130, 260), (257, 1000), (64, 4096)]
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("shape", SHAPES_C)
+def test_compress_bit_exact(dt, shape):
+    ss = lib()
+    M, K = shape
+    W = rand_bits(100 + M + K, shape, dt, 0.02 if dt != "f16" else 1.0)
+    values, meta, meta_hw = ss.sp24_prune_compress(dev_tensor(W, dt))
+    torch.cuda.synchronize()
+    v_ref, m_ref = oracle.sp24.compress(W, dt)
+    assert np.array_equal(bits_of(values), v_ref)
+    assert np.array_equal(bits_of(meta), m_ref)
+    assert np.array_equal(bits_of(meta_hw), oracle.sp24.meta_hw_from_canonical(m_ref, M, K, dt))
+    assert ss.check_device_error() == 0
+
+
+def test_compress_strided_input():
+    ss = lib()
+    M, K, ld = 70, 200, 264
+    big = rand_bits(5, (M, ld), "bf16")
+    Wt = dev_tensor(big, "bf16")[:, :K]
+    values, meta, meta_hw = ss.sp24_prune_compress(Wt)
+    v_ref, m_ref = oracle.sp24.compress(np.ascontiguousarray(big[:, :K]), "bf16")
+    assert np.array_equal(bits_of(values), v_ref) and np.array_equal(bits_of(meta), m_ref)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
+def test_compress_edge_values(dt):
+    ss = lib()
+    rng = np.random.default_rng(0)
+    if dt == "e4m3":
+        pool = np.array([0x00, 0x80, 0x01, 0x81, 0x07, 0x08, 0x38, 0xB8, 0x7E, 0xFE, 0x7D, 0x40], np.uint8)
+    else:
+        sgn = 0x8000
+        pool = np.array([0, sgn, 1, sgn | 1, 0x3FF, 0x400, 0x3C00, sgn | 0x3C00, 0x7BFF, sgn | 0x7BFF,
+                         0x3C01, 0x3BFF], np.uint16)
+    W = pool[rng.integers(0, len(pool), size=(96, 512))]
+    W[0, :] = pool[6]                       # all-equal groups
+    W[1, :] = 0                             # all-zero groups
+    values, meta, meta_hw = ss.sp24_prune_compress(dev_tensor(W, dt))
+    v_ref, m_ref = oracle.sp24.compress(W, dt)
+    assert np.array_equal(bits_of(values), v_ref)
+    assert np.array_equal(bits_of(meta), m_ref)
+
+
+GEMM_SHAPES = [(128, 256, 64), (200, 72, 136), (256, 512, 1024), (300, 40, 8), (64, 1000, 96), (384, 264, 520)]
+
+
+def _check_y(Y, Y_ref, B, out_dt, rel):
+    yb = bits_of(Y)
+    ok = oracle.gemm.within_bound(yb, Y_ref, B, out_dt, rel)
+    if not ok.all():
+        bad = np.argwhere(~ok)
+        i, j = bad[0]
+        y = oracle.codecs.decode(yb[i, j], out_dt)
+        r = oracle.codecs.decode(Y_ref[i, j], out_dt)
+        raise AssertionError(f"{(~ok).sum()} of {ok.size} outside the bound; first at {i},{j}: "
+                             f"gpu {y} ref {r} bound {B[i, j] * rel}")
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("shape", GEMM_SHAPES)
+def test_sp24_gemm_within_bound(dt, shape):
+    ss = lib()
+    M, N, K = shape
+    W = rand_bits(200 + M, (M, K), dt, 0.5)
+    X = rand_bits(300 + N, (K, N), dt, 1.0)
+    out_dt = "bf16" if dt == "e4m3" else dt
+    alpha = 0.75 if dt == "e4m3" else 1.0
+    values, meta, meta_hw = ss.sp24_prune_compress(dev_tensor(W, dt))
+    Y, buf = guarded_output(M, N, torch.bfloat16 if out_dt == "bf16" else torch.float16)
+    ss.sp24_gemm(values, meta_hw, dev_padded(X, dt), K, alpha=alpha, out=Y)
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
+    v_ref, m_ref = oracle.sp24.compress(W, dt)
+    Y_ref = oracle.gemm.gemm_sp24(v_ref, m_ref, K, X, dt, out_dt, alpha)
+    B = oracle.gemm.bound(oracle.sp24.decompress(v_ref, m_ref, K), X, dt, alpha)
+    _check_y(Y, Y_ref, B, out_dt, REL[dt])
+    assert canary_intact(buf, M, N)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("shape", GEMM_SHAPES)
+def test_dense_gemm_within_bound(dt, shape):
+    ss = lib()
+    M, N, K = shape
+    W = rand_bits(400 + M, (M, K), dt, 0.5)
+    X = rand_bits(500 + N, (K, N), dt, 1.0)
+    out_dt = "bf16" if dt == "e4m3" else dt
+    Y, buf = guarded_output(M, N, torch.bfloat16 if out_dt == "bf16" else torch.float16)
+    ss.dense_gemm(dev_padded(W, dt), dev_padded(X, dt), alpha=1.0, out=Y)
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
+    Y_ref = oracle.gemm.gemm_dense(W, X, dt, out_dt)
+    B = oracle.gemm.bound(W, X, dt)
+    _check_y(Y, Y_ref, B, out_dt, REL[dt])
+    assert canary_intact(buf, M, N)
+
+
+def test_sp24_gemm_identity_is_exact():
+    """X = I gives Y = the pruned W exactly (each output is a single product)."""
+    ss = lib()
+    M, K = 256, 256
+    W = rand_bits(9, (M, K), "bf16", 1.0)
+    X = oracle.codecs.encode(np.eye(K), "bf16")
+    values, _, meta_hw = ss.sp24_prune_compress(dev_tensor(W, "bf16"))
+    Y = ss.sp24_gemm(values, meta_hw, dev_tensor(X, "bf16"), K)
+    assert np.array_equal(bits_of(Y), oracle.sp24.prune(W, "bf16"))
+
+
+def test_k_zero_and_empty():
+    ss = lib()
+    X = torch.zeros((0, 16), dtype=torch.bfloat16, device="cuda")
+    Y = torch.full((8, 16), 3.0, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros((8, 0), dtype=torch.bfloat16, device="cuda")
+    m = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    ss.sp24_gemm(v, m, X, 0, out=Y)
+    assert (Y == 0).all()
+
+
+def test_two_calls_in_a_row_agree():
+    ss = lib()
+    M, N, K = 256, 256, 512
+    W = rand_bits(11, (M, K), "f16")
+    X = rand_bits(12, (K, N), "f16")
+    values, _, meta_hw = ss.sp24_prune_compress(dev_tensor(W, "f16"))
+    Xd = dev_tensor(X, "f16")
+    a = ss.sp24_gemm(values, meta_hw, Xd, K)
+    b = ss.sp24_gemm(values, meta_hw, Xd, K)
+    assert torch.equal(a, b)

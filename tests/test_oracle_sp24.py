@@ -138,14 +138,42 @@ def test_invariants(dt, shape):
         kpos = [p for p in range(4) if kept_mask[i, g, p] and tie[p]]
         dpos = [p for p in range(4) if (not kept_mask[i, g, p]) and tie[p]]
         assert max(kpos) < min(dpos)
-    # 4. hardware-blocked metadata is a pure re-blocking of the canonical bytes
-    hw = sp24.meta_hw_from_canonical(meta, M, K)
-    assert hw.size == sp24.meta_hw_size(M, K)
-    MB, KB = (M + 127) // 128, (K + 127) // 128
-    blocks = hw.reshape(MB, KB, 128, 16)
-    for i in range(0, M, max(1, M // 7)):
-        for byte in range(meta.shape[1]):
-            assert blocks[i // 128, byte // 16, i % 128, byte % 16] == meta[i, byte]
+    # 4. the hardware-ordered metadata is a permutation of the canonical nibbles
+    hw = sp24.meta_hw_from_canonical(meta, M, K, dt)
+    assert hw.size == sp24.meta_hw_size(M, K, dt)
+    assert (_canonical_from_hw(hw, M, K, dt)[:, :meta.shape[1]] == meta).all()
+
+
+def _canonical_from_hw(hw, M, K, dt):
+    """Independent inverse of the operand layout: rebuild canonical bytes row by row."""
+    MB = (M + 127) // 128
+    if dt == "e4m3":
+        KB = (K + 127) // 128
+        b = hw.reshape(MB, KB, 128, 16)
+        out = np.zeros((MB * 128, KB * 16), np.uint8)
+        for mb in range(MB):
+            for kb in range(KB):
+                out[mb * 128:(mb + 1) * 128, kb * 16:(kb + 1) * 16] = b[mb, kb]
+        return out[:M]
+    KB = (K + 63) // 64
+    w = hw.view("<u4").reshape(MB, KB, 128, 4)
+    out = np.zeros((MB * 128, KB * 2), np.uint32)
+    for mb in range(MB):
+        for kb in range(KB):
+            for j in range(2):
+                col = w[mb, kb, :, 2 * j]
+                assert (w[mb, kb, :, 2 * j + 1] == 0).all()
+                for r in range(128):
+                    lo, hi = int(col[r]) & 0xFFFF, int(col[r]) >> 16
+                    low_row = r & ~8
+                    up_row = r | 8
+                    if r & 8 == 0:    # groups 0..3 of rows r (low) and r + 8 (high)
+                        out[mb * 128 + low_row, 2 * kb + j] |= lo
+                        out[mb * 128 + up_row, 2 * kb + j] |= hi
+                    else:             # groups 4..7 of rows r - 8 (low) and r (high)
+                        out[mb * 128 + low_row, 2 * kb + j] |= lo << 16
+                        out[mb * 128 + up_row, 2 * kb + j] |= hi << 16
+    return out.view(np.uint8).reshape(MB * 128, -1)[:M]
 
 
 def test_all_equal_and_signed_zero_groups():

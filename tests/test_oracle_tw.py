@@ -100,6 +100,10 @@ def test_layout_invariants_and_unpack(tvw):
             assert (blk == dense).all()
     assert list(f["schedule"]) == [2, 0, 1]
     R = tw.padded(keep.astype(np.int64))
+    P = [0, R[0], R[0] + R[1]]
+    Q = [0, (R[0] + 127) // 128, (R[0] + 127) // 128 + (R[1] + 127) // 128]
+    assert list(f["schedule_table"]) == [2, keep[2], P[2], Q[2], 0, keep[0], P[0], Q[0], 1, keep[1], P[1], Q[1]]
+    R = tw.padded(keep.astype(np.int64))
     assert f["packed"].size == 128 * R.sum() // (2 if tvw else 1)
 
 
@@ -113,8 +117,7 @@ def test_tvw_equals_sp24_on_packed_tile():
     packed = f["packed"].reshape(1, 128, 32)[0]            # one 64-column chunk
     assert (packed == v[:, :32]).all()
     assert (f["meta"].reshape(128, 8) == m[:, :8]).all()
-    hw = f["meta_hw"].reshape(128, 16)
-    assert (hw[:, :8] == m[:, :8]).all() and (hw[:, 8:] == 0x44).all()
+    assert (f["meta_hw"] == sp24.meta_hw_from_canonical(m[:, :8], 128, 64, "bf16")).all()
 
 
 def test_full_keep_reduces_to_dense_and_empty_gives_zero():
