@@ -1,0 +1,391 @@
+"""Benchmark of the structured-sparse GEMM path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One JSON line on rank 0. A step is one sparse GEMM Y = W_sparse . X over the
+workload's activation batch, with the 2:4-compressed weight resident in HBM
+(weights are pruned and compressed once; the per-step work is the GEMM). L2 is
+flushed (a 256 MB write) between timed steps; each step is timed with CUDA
+events on the launching stream. The other hot-path rows (prune/compress, the
+tile-wise prune, the TW/TVW gather GEMMs and the dense GEMM of the same kernel
+family) are timed the same way and reported under "rows".
+
+--impl reference times the CPU oracle (the test suite's reference
+implementation) on this host's cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from structured_sparse_dnn_gb300 import inputs as I  # noqa: E402
+
+METRIC = "effective TFLOP/s and % of 2:4-sparse tensor peak for sparse GEMM (1×GB300)"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "llm_ffn_e4m3"
+FLUSH_BYTES = 256 << 20
+
+
+def peaks() -> dict:
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in m})
+        p["source"] = "measured"
+    return p
+
+
+def tensor_peak_effective(dt: str, pk: dict, sustained: bool = False) -> float:
+    """2:4-sparse tensor peak in effective (nonzero) TFLOP/s: the sparse core runs
+    twice the dense-equivalent rate, i.e. one dense peak of nonzero MACs. e4m3 is
+    twice bf16 (nominal ratio)."""
+    base = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+    return base * (2.0 if dt == "e4m3" else 1.0)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier_max(value: float, ws: int) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_steps(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> list[float]:
+    """ms per step: warmup untimed calls, then `steps` calls each between an L2
+    flush and a pair of CUDA events on `stream`."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def make_sp24(wl, dev, ss):
+    d = wl.make()
+    Wd = I.torch_view(d["W"], wl.dt).to(dev)
+    Xd = I.torch_view(d["X"], wl.dt).to(dev)
+    values, meta, meta_hw = ss.sp24_prune_compress(Wd, canonical_meta=False)
+    return d, Wd, Xd, values, meta_hw
+
+
+def run_gpu(args) -> None:
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from structured_sparse_dnn_gb300 import build
+    if rank == 0 or not os.path.exists(build.LIB):
+        build.build()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    from structured_sparse_dnn_gb300 import ssdnn
+
+    pk = peaks()
+    wl = I.WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    d, Wd, Xd, values, meta_hw = make_sp24(wl, dev, ss)
+    M, K, N = wl.M, wl.K, wl.N
+    Y = torch.empty((M, N), dtype=torch.bfloat16 if wl.out_dt == "bf16" else torch.float16, device=dev)
+    alpha = d["alpha"]
+    eff_flops = 2.0 * M * N * K * 0.5
+
+    def step():
+        ss.sp24_gemm(values, meta_hw, Xd, K, alpha=alpha, out=Y)
+
+    # ---- timed region: K steps, barrier + synchronize on both sides, clocks sampled
+    # (the sampler also covers about half a second of untimed warm-up GEMMs so that
+    # it sees the GPU under load)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 0.5:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+        times = timed_steps(step, args.steps, 0, flush, stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    assert ss.check_device_error() == 0, "device error flag set"
+    ms_total = barrier_max(sum(times), ws)
+    ms_step = ms_total / args.steps
+    value = ws * eff_flops * args.steps / (ms_total * 1e-3) / 1e12
+    kernel_ms = statistics.mean(times)
+    achieved = eff_flops / (kernel_ms * 1e-3) / 1e12
+    peak_eff = tensor_peak_effective(wl.dt, pk)
+
+    # ---- end to end through the public call with host buffers (pinned)
+    X_host = I.torch_view(d["X"], wl.dt).pin_memory()
+    Y_host = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+
+    def e2e_step():
+        Xd.copy_(X_host, non_blocking=True)
+        step()
+        Y_host.copy_(Y, non_blocking=True)
+
+    e2e_times = timed_steps(e2e_step, max(3, args.steps // 2), 2, flush, stream)
+    e2e_value = ws * eff_flops / (statistics.mean(e2e_times) * 1e-3) / 1e12
+
+    rows = {}
+    if not args.no_rows and rank == 0:
+        rows = bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, values, Xd)
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dt, "data": "synthetic (seeded generator)",
+            "config": {"workload": f"{wl.name}: W {M}x{K} N(0,{wl.sigma_w:g}) pruned 2:4, X {K}x{N} N(0,1), "
+                                   f"{wl.dt} in, {wl.out_dt} out, fp32 accumulate",
+                       "M": M, "K": K, "N": N, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "l2": "flushed between timed steps (256 MB write)"},
+            "pct_of_sparse_peak": round(100.0 * achieved / peak_eff, 2),
+            "dense_equivalent_tflops": round(2 * achieved, 2),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak_eff, 1),
+                         "unit": "TFLOP/s", "frac": round(achieved / peak_eff, 4), "traffic": None,
+                         "peak_note": f"2:4-sparse {wl.dt} peak in nonzero-MAC TFLOP/s = "
+                                      f"{'2 x ' if wl.dt == 'e4m3' else ''}{pk['source']} bf16 dense burst "
+                                      f"{pk['bf16_tflops']}"},
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": int(Xd.numel() * Xd.element_size()),
+                    "d2h_bytes_per_step": int(Y.numel() * Y.element_size())},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "rows": rows,
+        }
+        if args.cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, d, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, values, Xd) -> dict:
+    """Time the other hot-path rows on their own workloads."""
+    rows = {}
+    steps = max(5, args.steps // 2)
+    M, K, N = wl.M, wl.K, wl.N
+    eb = I.ELEM_BYTES[wl.dt]
+    vb, mb, hb = ss.sp24_sizes(ss._DT[Wd.dtype], M, K)
+    # a1: prune + compress (HBM bound): read W, write values + canonical meta + operand meta
+    t = statistics.mean(timed_steps(lambda: ss.sp24_prune_compress(Wd), steps, 2, flush, stream))
+    nbytes = M * K * eb + vb + mb + hb
+    rows["sp24_prune_compress"] = {"workload": wl.name, "ms": round(t, 4), "GB/s": round(nbytes / t / 1e6, 1),
+                                   "frac_of_hbm": round(nbytes / t / 1e6 / pk["hbm_gbs"], 3)}
+    # a8: the dense GEMM of the same kernel family on the same shape
+    Yd = torch.empty((M, N), dtype=torch.bfloat16 if wl.out_dt == "bf16" else torch.float16, device=dev)
+    t = statistics.mean(timed_steps(lambda: ss.dense_gemm(Wd, Xd, alpha=d["alpha"], out=Yd), steps, 2, flush,
+                                    stream))
+    dense_tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
+    rows["dense_gemm"] = {"workload": wl.name, "ms": round(t, 4), "TFLOP/s": round(dense_tf, 1),
+                          "frac_of_dense_peak": round(dense_tf / (pk["bf16_tflops"] * (2 if wl.dt == "e4m3" else 1)),
+                                                      3)}
+    # a2 in bf16 on the same LLM FFN shape, when the headline is e4m3
+    if wl.name == "llm_ffn_e4m3":
+        wb = I.WORKLOADS["llm_ffn_bf16"]
+        db, Wb, Xb, vb16, hb16 = make_sp24(wb, dev, ss)
+        Yb = torch.empty((wb.M, wb.N), dtype=torch.bfloat16, device=dev)
+        t = statistics.mean(timed_steps(lambda: ss.sp24_gemm(vb16, hb16, Xb, wb.K, out=Yb), steps, 2, flush,
+                                        stream))
+        eff = wb.M * wb.N * wb.K / (t * 1e-3) / 1e12
+        rows["sp24_gemm_bf16"] = {"workload": wb.name, "ms": round(t, 4), "effective_TFLOP/s": round(eff, 1),
+                                  "dense_equivalent_TFLOP/s": round(2 * eff, 1),
+                                  "frac_of_sparse_bf16_peak": round(eff / pk["bf16_tflops"], 4)}
+        t = statistics.mean(timed_steps(lambda: ss.dense_gemm(Wb, Xb, out=Yb), steps, 2, flush, stream))
+        rows["dense_gemm_bf16"] = {"workload": wb.name, "ms": round(t, 4),
+                                   "TFLOP/s": round(2.0 * wb.M * wb.N * wb.K / (t * 1e-3) / 1e12, 1)}
+        del db, Wb, Xb, vb16, hb16, Yb
+    # a3-a7: tile-wise prune and the TW / TVW gather GEMMs vs the same-kernel dense GEMM
+    tw = I.WORKLOADS["tile_wise_4096_bf16"]
+    dt_ = tw.make()
+    keep = dt_["keep"]
+    keep4 = (keep // 4) * 4
+    Wt = I.torch_view(dt_["W"], "bf16").to(dev)
+    Xt = I.torch_view(dt_["X"], "bf16").to(dev)
+    Yt = torch.empty((tw.M, tw.N), dtype=torch.bfloat16, device=dev)
+    sz = ss.tw_sizes(ss.BF16, True, tw.M, tw.K, keep4)
+    work = torch.empty(sz["workspace_bytes"], dtype=torch.uint8, device=dev)
+    t_prune = statistics.mean(timed_steps(lambda: ss.tw_prune_compress(Wt, keep4, True, work), steps, 2, flush,
+                                          stream))
+    form_tvw = ss.tw_prune_compress(Wt, keep4, True, work)
+    form_tw = ss.tw_prune_compress(Wt, keep, False, work)
+    t_tw = statistics.mean(timed_steps(lambda: ss.tvw_gemm(form_tw, Xt, out=Yt), steps, 2, flush, stream))
+    t_tvw = statistics.mean(timed_steps(lambda: ss.tvw_gemm(form_tvw, Xt, out=Yt), steps, 2, flush, stream))
+    t_dense = statistics.mean(timed_steps(lambda: ss.dense_gemm(Wt, Xt, out=Yt), steps, 2, flush, stream))
+    dens = keep.sum() / (tw.M * tw.K / 128) / 128
+    flops_tw = 2.0 * 128 * float(keep.sum()) * tw.N
+    flops_tvw = 2.0 * 128 * float(keep4.sum()) * tw.N * 0.5
+    rows["tile_wise"] = {
+        "workload": tw.name, "kept_fraction": round(float(keep.sum()) / tw.K / len(keep), 4),
+        "tw_prune_compress_ms (TVW)": round(t_prune, 4),
+        "tw_gemm_ms": round(t_tw, 4), "tw_effective_TFLOP/s": round(flops_tw / (t_tw * 1e-3) / 1e12, 1),
+        "tvw_gemm_ms": round(t_tvw, 4), "tvw_effective_TFLOP/s": round(flops_tvw / (t_tvw * 1e-3) / 1e12, 1),
+        "dense_gemm_ms": round(t_dense, 4),
+        "dense_TFLOP/s": round(2.0 * tw.M * tw.N * tw.K / (t_dense * 1e-3) / 1e12, 1),
+        "tvw_speedup_over_dense": round(t_dense / t_tvw, 3), "tw_speedup_over_dense": round(t_dense / t_tw, 3),
+        "sparsity": round(1 - float(dens), 4),
+    }
+    return rows
+
+
+def cpu_baseline(wl, d, seconds: float) -> dict:
+    """The CPU oracle, as it stands, on a bounded row sample of the workload."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    rows = 64
+    elapsed = 0.0
+    done_rows = 0
+    rng = np.random.default_rng(0)
+    while elapsed < seconds and done_rows < wl.M:
+        sel = np.sort(rng.choice(wl.M, size=min(rows, wl.M), replace=False))
+        t0 = time.perf_counter()
+        v, m = oracle.sp24.compress(d["W"][sel], wl.dt)
+        oracle.gemm.gemm_sp24(v, m, wl.K, d["X"], wl.dt, wl.out_dt, d["alpha"])
+        elapsed += time.perf_counter() - t0
+        done_rows += len(sel)
+        rows *= 2
+    eff = 2.0 * done_rows * wl.N * wl.K * 0.5 / elapsed / 1e12
+    return {"value": eff, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done_rows} random rows of W (all N={wl.N} columns, K={wl.K}); prune + compress + "
+                      f"decompress + fp64 matmul + rounding, {elapsed:.1f} s"}
+
+
+def run_reference(args) -> None:
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    wl = I.WORKLOADS[args.workload]
+    d = wl.make()
+    import oracle  # noqa: F401
+    cores = len(os.sched_getaffinity(0))
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    times, rows_done = [], []
+    for i in range(args.warmup + args.steps):
+        b = cpu_baseline(wl, d, per_step)
+        if i >= args.warmup:
+            times.append(b)
+    value = statistics.mean(b["value"] for b in times)
+    ms = statistics.mean(2.0 * wl.M * wl.N * wl.K * 0.5 / (b["value"] * 1e12) * 1e3 for b in times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dt, "data": "synthetic (seeded generator)",
+            "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": times[-1]["sample"] + " per step (throughput scaled to the full workload)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row sub-benchmarks")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
