@@ -115,12 +115,20 @@ def dist_env():
 
 
 def barrier_max(value: float, ws: int) -> float:
+    """Max of a per-rank scalar over all ranks (identity on one rank)."""
     if ws == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_step_per_rank: float, steps: int, ms_total_max: float, ws: int) -> float:
+    """Weak scaling: every rank runs its own steps; the job's throughput is all
+    ranks' work over the slowest rank's time."""
+    return ws * flops_per_step_per_rank * steps / (ms_total_max * 1e-3) / 1e12
 
 
 def timed_steps(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> list[float]:
@@ -163,7 +171,7 @@ def run_gpu(args) -> None:
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
-    from structured_sparse_dnn_gb300 import ssdnn
+    from structured_sparse_dnn_gb300 import ssdnn as ss
 
     pk = peaks()
     wl = I.WORKLOADS[args.workload]
@@ -200,7 +208,7 @@ def run_gpu(args) -> None:
     assert ss.check_device_error() == 0, "device error flag set"
     ms_total = barrier_max(sum(times), ws)
     ms_step = ms_total / args.steps
-    value = ws * eff_flops * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(eff_flops, args.steps, ms_total, ws)
     kernel_ms = statistics.mean(times)
     achieved = eff_flops / (kernel_ms * 1e-3) / 1e12
     peak_eff = tensor_peak_effective(wl.dt, pk)
@@ -305,7 +313,7 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, values, Xd) -> dict:
     t_tw = statistics.mean(timed_steps(lambda: ss.tvw_gemm(form_tw, Xt, out=Yt), steps, 2, flush, stream))
     t_tvw = statistics.mean(timed_steps(lambda: ss.tvw_gemm(form_tvw, Xt, out=Yt), steps, 2, flush, stream))
     t_dense = statistics.mean(timed_steps(lambda: ss.dense_gemm(Wt, Xt, out=Yt), steps, 2, flush, stream))
-    dens = keep.sum() / (tw.M * tw.K / 128) / 128
+    dens = 128.0 * keep.sum() / (tw.M * tw.K)
     flops_tw = 2.0 * 128 * float(keep.sum()) * tw.N
     flops_tvw = 2.0 * 128 * float(keep4.sum()) * tw.N * 0.5
     rows["tile_wise"] = {
