@@ -147,6 +147,37 @@ int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* ke
              const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
              const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream);
 
+/* ------------------------------------------------- allocation-free variant ----
+ * tw_prune_compress_noalloc: tw_prune_compress for callers that cannot allocate
+ * device memory. (The pages have no counterpart: this is a deployment aid.)
+ * Who needs it: a plugin running inside an inference engine that owns all device
+ * memory and hands it only the buffers of its inputs and outputs, or a serving
+ * loop that must never call cudaMalloc/cudaFree, which synchronise the device
+ * and can fail under memory pressure. Such callers cannot provide the score
+ * workspace tw_prune_compress needs.
+ * What it does instead: the per-tile scores go to a fixed array in device memory
+ * that the library defines (SSDNN_NOALLOC_MAX_SCORES floats = 8 MiB); every GPU
+ * that loads the library holds that array until the process exits. The offsets
+ * and schedule tables are computed on the device, so no host-to-device copy is
+ * made either. The call allocates nothing and calls no allocating routine.
+ * Limits: nt = ceil(M/128) <= SSDNN_NOALLOC_MAX_TILES and nt * K <=
+ * SSDNN_NOALLOC_MAX_SCORES; beyond them it returns SSDNN_ERR_UNSUPPORTED and does
+ * nothing.
+ * Set-up: the first call on each device looks up the device address of that
+ * array (with the device current); make that first call before any stream
+ * capture.
+ * Sharing: all calls on a device share the one array, which keeps the last call's
+ * scores (every call overwrites the part it reads, so nothing needs clearing).
+ * Calls whose work overlaps on the GPU (different streams without ordering) race
+ * on it and must be serialised by the caller.
+ * Arguments, layouts and results are those of tw_prune_compress (bit-identical
+ * outputs), without the workspace. */
+#define SSDNN_NOALLOC_MAX_SCORES (1 << 21)
+#define SSDNN_NOALLOC_MAX_TILES 2048
+int tw_prune_compress_noalloc(int dt, int tvw, const void* W, int64_t M, int64_t K, int64_t ldw,
+                              const int32_t* keep_counts_host, int32_t* offsets, int32_t* indices,
+                              int32_t* schedule, void* packed, uint8_t* meta, uint8_t* meta_hw, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

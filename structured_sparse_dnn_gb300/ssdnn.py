@@ -42,6 +42,8 @@ _SIGS = {
                            _ptr, _ptr], C.c_int),
     "tvw_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _ptr,
                   _i64, _ptr], C.c_int),
+    "tw_prune_compress_noalloc": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr,
+                                   _ptr, _ptr], C.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -180,6 +182,33 @@ def tw_prune_compress(W: torch.Tensor, keep, tvw: bool, workspace: torch.Tensor 
     _check(lib.tw_prune_compress(dt, int(tvw), _p(W), M, K, W.stride(0), _kp(k), _p(offsets), _p(indices),
                                  _p(schedule), _p(packed), _p(meta), _p(meta_hw), _p(workspace), _stream(dev)),
            "tw_prune_compress")
+    return TileWise(dt, tvw, M, K, k, offsets, indices[:sz["indices_count"]], schedule[:4 * nt],
+                    packed[:sz["packed_bytes"] // 2],
+                    None if meta is None else meta[:sz["meta_bytes"]],
+                    None if meta_hw is None else meta_hw[:sz["meta_hw_bytes"]])
+
+
+def tw_prune_compress_noalloc(W: torch.Tensor, keep, tvw: bool) -> TileWise:
+    """tw_prune_compress without a workspace: for callers that cannot allocate
+    device memory inside the call. The library keeps the score scratch in a fixed
+    device array (8 MiB, shared by all calls on a device; overlapping calls race).
+    The output tensors here are still allocated by this Python helper."""
+    dt = _DT[W.dtype]
+    M, K = W.shape
+    assert W.stride(1) == 1
+    k = _keep_arr(keep)
+    sz = tw_sizes(dt, tvw, M, K, k)
+    dev = W.device
+    nt = (M + 127) // 128
+    offsets = torch.empty(nt + 1, dtype=torch.int32, device=dev)
+    indices = torch.empty(max(1, sz["indices_count"]), dtype=torch.int32, device=dev)
+    schedule = torch.empty(4 * max(1, nt), dtype=torch.int32, device=dev)
+    packed = torch.empty(max(8, sz["packed_bytes"] // 2), dtype=W.dtype, device=dev)
+    meta = torch.empty(max(16, sz["meta_bytes"]), dtype=torch.uint8, device=dev) if tvw else None
+    meta_hw = torch.empty(max(16, sz["meta_hw_bytes"]), dtype=torch.uint8, device=dev) if tvw else None
+    _check(lib.tw_prune_compress_noalloc(dt, int(tvw), _p(W), M, K, W.stride(0), _kp(k), _p(offsets), _p(indices),
+                                         _p(schedule), _p(packed), _p(meta), _p(meta_hw), _stream(dev)),
+           "tw_prune_compress_noalloc")
     return TileWise(dt, tvw, M, K, k, offsets, indices[:sz["indices_count"]], schedule[:4 * nt],
                     packed[:sz["packed_bytes"] // 2],
                     None if meta is None else meta[:sz["meta_bytes"]],
