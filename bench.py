@@ -154,8 +154,8 @@ def make_sp24(wl, dev, ss):
     d = wl.make()
     Wd = I.torch_view(d["W"], wl.dt).to(dev)
     Xd = I.torch_view(d["X"], wl.dt).to(dev)
-    values, meta, meta_hw = ss.sp24_prune_compress(Wd, canonical_meta=False)
-    return d, Wd, Xd, values, meta_hw
+    form = ss.sp24_prune_compress(Wd, canonical_meta=False)
+    return d, Wd, Xd, form
 
 
 def run_gpu(args) -> None:
@@ -177,14 +177,14 @@ def run_gpu(args) -> None:
     wl = I.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    d, Wd, Xd, values, meta_hw = make_sp24(wl, dev, ss)
+    d, Wd, Xd, form = make_sp24(wl, dev, ss)
     M, K, N = wl.M, wl.K, wl.N
     Y = torch.empty((M, N), dtype=torch.bfloat16 if wl.out_dt == "bf16" else torch.float16, device=dev)
     alpha = d["alpha"]
     eff_flops = 2.0 * M * N * K * 0.5
 
     def step():
-        ss.sp24_gemm(values, meta_hw, Xd, K, alpha=alpha, out=Y)
+        ss.sp24_gemm(form, Xd, alpha=alpha, out=Y)
 
     # ---- timed region: K steps, barrier + synchronize on both sides, clocks sampled
     # (the sampler also covers about half a second of untimed warm-up GEMMs so that
@@ -227,7 +227,7 @@ def run_gpu(args) -> None:
 
     rows = {}
     if not args.no_rows and rank == 0:
-        rows = bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, values, Xd)
+        rows = bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd)
 
     if rank == 0:
         clocks = clk.summary()
@@ -261,16 +261,16 @@ def run_gpu(args) -> None:
         dist.destroy_process_group()
 
 
-def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, values, Xd) -> dict:
+def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd) -> dict:
     """Time the other hot-path rows on their own workloads."""
     rows = {}
     steps = max(5, args.steps // 2)
     M, K, N = wl.M, wl.K, wl.N
     eb = I.ELEM_BYTES[wl.dt]
     vb, mb, hb = ss.sp24_sizes(ss._DT[Wd.dtype], M, K)
-    # a1: prune + compress (HBM bound): read W, write values + canonical meta + operand meta
-    t = statistics.mean(timed_steps(lambda: ss.sp24_prune_compress(Wd), steps, 2, flush, stream))
-    nbytes = M * K * eb + vb + mb + hb
+    # a1: prune + compress (HBM bound): read W, write values + operand-order metadata
+    t = statistics.mean(timed_steps(lambda: ss.sp24_prune_compress(Wd, canonical_meta=False), steps, 2, flush, stream))
+    nbytes = M * K * eb + vb + hb
     rows["sp24_prune_compress"] = {"workload": wl.name, "ms": round(t, 4), "GB/s": round(nbytes / t / 1e6, 1),
                                    "frac_of_hbm": round(nbytes / t / 1e6 / pk["hbm_gbs"], 3)}
     # a8: the dense GEMM of the same kernel family on the same shape
@@ -284,10 +284,9 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, values, Xd) -> dict:
     # a2 in bf16 on the same LLM FFN shape, when the headline is e4m3
     if wl.name == "llm_ffn_e4m3":
         wb = I.WORKLOADS["llm_ffn_bf16"]
-        db, Wb, Xb, vb16, hb16 = make_sp24(wb, dev, ss)
+        db, Wb, Xb, fb = make_sp24(wb, dev, ss)
         Yb = torch.empty((wb.M, wb.N), dtype=torch.bfloat16, device=dev)
-        t = statistics.mean(timed_steps(lambda: ss.sp24_gemm(vb16, hb16, Xb, wb.K, out=Yb), steps, 2, flush,
-                                        stream))
+        t = statistics.mean(timed_steps(lambda: ss.sp24_gemm(fb, Xb, out=Yb), steps, 2, flush, stream))
         eff = wb.M * wb.N * wb.K / (t * 1e-3) / 1e12
         rows["sp24_gemm_bf16"] = {"workload": wb.name, "ms": round(t, 4), "effective_TFLOP/s": round(eff, 1),
                                   "dense_equivalent_TFLOP/s": round(2 * eff, 1),
@@ -295,7 +294,7 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, values, Xd) -> dict:
         t = statistics.mean(timed_steps(lambda: ss.dense_gemm(Wb, Xb, out=Yb), steps, 2, flush, stream))
         rows["dense_gemm_bf16"] = {"workload": wb.name, "ms": round(t, 4),
                                    "TFLOP/s": round(2.0 * wb.M * wb.N * wb.K / (t * 1e-3) / 1e12, 1)}
-        del db, Wb, Xb, vb16, hb16, Yb
+        del db, Wb, Xb, fb, Yb
     # a3-a7: tile-wise prune and the TW / TVW gather GEMMs vs the same-kernel dense GEMM
     tw = I.WORKLOADS["tile_wise_4096_bf16"]
     dt_ = tw.make()

@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -47,8 +48,10 @@ namespace {
 
 struct Params {
   int32_t M, N;
-  int32_t MB, NB;           // 128-row blocks, BN-column blocks
-  int32_t num_units;
+  int32_t MB, NB;           // BM-row blocks (BM = 128 MT), BN-column blocks
+  int32_t MB128;            // 128-row blocks (the metadata's row blocks)
+  int32_t MG;               // groups of CS consecutive BM-row blocks (one group per cluster pass)
+  int32_t num_units;        // work items: (M group, N block) pairs, or (schedule entry, N block)
   int32_t nk;               // k stages per unit (dense / sp24)
   int32_t out_dt;           // 0 f16, 1 bf16
   float alpha;
@@ -61,14 +64,19 @@ struct Params {
   uint32_t* err;
 };
 
-template <int DT, bool SPARSE, bool GATHER, int BN>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT>
 struct Cfg {
+  static constexpr int CLUSTER = CS;                        // CTAs sharing one X panel by multicast
+  static constexpr int SUB = MT;                            // 128-row sub-tiles per CTA tile
+  static constexpr int BM = 128 * MT;
+  static constexpr int THREADS = 128 + 128 * MT;            // 4 control warps + 4 epilogue warps per sub-tile
   static constexpr int EB = Elem<DT>::bytes;
   static constexpr bool F8 = Elem<DT>::f8;
   static constexpr int BK = 128 / EB;                       // dense K per stage
-  static constexpr int A_BYTES = SPARSE ? 128 * 64 : 128 * 128;
+  static constexpr int A_SUB_BYTES = SPARSE ? 128 * 64 : 128 * 128;
+  static constexpr int A_BYTES = MT * A_SUB_BYTES;
   static constexpr int B_BYTES = 128 * BN;                  // BK * BN * EB
-  static constexpr int META_BYTES = SPARSE ? 2048 : 0;
+  static constexpr int META_BYTES = SPARSE ? 2048 * MT : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + META_BYTES;
   static constexpr int STAGES_RAW = (220 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -77,19 +85,28 @@ struct Cfg {
   static constexpr int B_BOX_COLS = 128 / EB;                // columns per 128-byte B box
   static constexpr int B_BOXES = BN / B_BOX_COLS;
   static constexpr int B_BOX_BYTES = BK * 128;
-  static constexpr int NACC = (BN >= 256) ? 1 : 2;
-  static constexpr int META_COL0 = 256;                      // TMEM columns 256.. hold metadata
+  static constexpr int ACC_COLS = MT * BN;                  // fp32 accumulator columns of one tile
   static constexpr int META_SLOTS = 4;
+  static constexpr int META_SLOT_COLS = 4 * MT;             // one 128x128b copy per sub-tile
+  static constexpr int META_COLS = SPARSE ? META_SLOTS * META_SLOT_COLS : 0;
+  static constexpr int NACC = (2 * ACC_COLS + META_COLS <= 512) ? 2 : 1;
+  static constexpr int META_COL0 = NACC * ACC_COLS;         // TMEM columns after the accumulators
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC = ptx::idesc(Elem<DT>::mma_fmt, Elem<DT>::mma_fmt, SPARSE, 128, BN,
                                                false, true);
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(B_BOXES * B_BOX_COLS == BN, "BN must be a multiple of the 128-byte box width");
-  static_assert(NACC * BN <= META_COL0, "accumulators overlap the metadata columns");
+  static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
+  static_assert(MT == 1 || (CS == 1 && !GATHER), "256-row tiles: no cluster, no gather");
+  static_assert(CS == 1 || !GATHER, "gathered B rows differ per tile: no multicast");
+  static constexpr int B_SLICE_ROWS = BK / CS;              // rows of each B box this CTA loads
+  static_assert(B_SLICE_ROWS % 8 == 0, "B slices must keep whole 8-row swizzle atoms");
 };
 
 struct UnitInfo {
   int32_t m0, n0, nk;
+  int32_t subs;       // 128-row sub-tiles of this tile that hold rows of W (the rest are zero)
+  bool phantom;       // a cluster member past the last 128-row block: loads B, writes nothing
   int32_t a_row0;     // packed-operand row of the first chunk (TW/TVW)
   int32_t meta_blk0;  // first metadata block index
   int32_t idx_base;   // offsets[t] (TW/TVW)
@@ -97,21 +114,27 @@ struct UnitInfo {
 };
 
 template <typename C, bool GATHER>
-__device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u) {
+__device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint32_t crank) {
   UnitInfo ui;
   if constexpr (!GATHER) {
-    const int32_t mb = u % p.MB, nb = u / p.MB;
-    ui.m0 = mb * 128;
+    const int32_t mg = u % p.MG, nb = u / p.MG;
+    const int32_t mb = mg * C::CLUSTER + static_cast<int32_t>(crank);
+    ui.phantom = mb >= p.MB;
+    ui.m0 = mb * C::BM;
     ui.n0 = nb * (C::B_BOXES * C::B_BOX_COLS);
     ui.nk = p.nk;
     ui.a_row0 = ui.m0;
-    ui.meta_blk0 = mb * p.nk;  // one 2048-byte metadata block per stage
+    // one 2048-byte metadata block per (128-row block, stage)
+    ui.meta_blk0 = mb * C::SUB * p.nk;
+    ui.subs = ui.phantom ? 0 : min(C::SUB, p.MB128 - mb * C::SUB);
     ui.idx_base = 0;
     ui.L = 0;
   } else {
     const int32_t e = u / p.NB, nb = u % p.NB;
     const int32_t* s = p.schedule + 4 * e;
     const int32_t t = __ldg(s + 0), L = __ldg(s + 1), P = __ldg(s + 2), Q = __ldg(s + 3);
+    ui.phantom = false;
+    ui.subs = 1;
     ui.m0 = t * 128;
     ui.n0 = nb * (C::B_BOXES * C::B_BOX_COLS);
     ui.nk = (L + C::BK - 1) / C::BK;
@@ -123,10 +146,18 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u) {
   return ui;
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN>
-__global__ void __launch_bounds__(256, 1)
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT>
+__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = Cfg<DT, SPARSE, GATHER, BN>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT>;
+  // Clusters of CS CTAs along M share each X panel: CTA rank r loads rows
+  // [r BK/CS, (r+1) BK/CS) of every B box of a stage and multicasts them to the
+  // whole cluster, so a stage is complete only when all CS slices have landed and
+  // can be refilled only when all CS MMA issuers have released it.
+  const uint32_t crank = (CS > 1) ? ptx::cluster_ctarank() : 0u;
+  const int32_t unit0 = static_cast<int32_t>(blockIdx.x) / CS;
+  const int32_t unit_stride = static_cast<int32_t>(gridDim.x) / CS;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CS) - 1u);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -145,11 +176,11 @@ __global__ void __launch_bounds__(256, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], CS);
     }
     for (int a = 0; a < C::NACC; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], 128);
+      ptx::mbar_init(&acc_empty[a], 128 * MT);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -164,7 +195,10 @@ __global__ void __launch_bounds__(256, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (CS > 1)
+    ptx::cluster_sync();  // peers' barriers are initialised before any multicast reaches them
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -176,8 +210,24 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t phase = 0;
     int issued = 0;
     bool ok = true;
-    for (int32_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const UnitInfo ui = decode_unit<C, GATHER>(p, u);
+    // TW/TVW: ring of the X row indices of the next kIdxAhead stages (lanes 0..15)
+    constexpr int kIdxAhead = 4;
+    int32_t idx_ring[kIdxAhead][4];
+    auto load_idx = [&](const UnitInfo& ui, int32_t kb, int32_t (&r)[4]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int32_t j = kb * C::BK + 4 * static_cast<int32_t>(lane) + q;
+        r[q] = (kb < ui.nk && j < ui.L) ? __ldg(p.indices + ui.idx_base + j) : 0;
+      }
+    };
+    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
+      if constexpr (GATHER) {
+        if (lane < C::BK / 4) {
+#pragma unroll
+          for (int d = 0; d < kIdxAhead; ++d) load_idx(ui, d, idx_ring[d]);
+        }
+      }
       for (int32_t kb = 0; kb < ui.nk; ++kb) {
         if (*abort_flag) { ok = false; break; }
         if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, p.err);
@@ -186,45 +236,66 @@ __global__ void __launch_bounds__(256, 1)
         uint8_t* sA = smem + stage * C::STAGE_BYTES;
         uint8_t* sB = sA + C::A_BYTES;
         uint8_t* sM = sB + C::B_BYTES;
-        constexpr bool meta_now = SPARSE;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full[stage],
-                                     C::A_BYTES + C::B_BYTES + (meta_now ? C::META_BYTES : 0));
-          // A: dense W / 2:4 values box (inner coordinate in elements)
+          ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES + (SPARSE ? 2048 * ui.subs : 0));
+          // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
+          // rows past M read as zeros
           const int32_t a_col = GATHER ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
           const int32_t a_row = GATHER ? ui.a_row0 + 128 * kb : ui.m0;
           ptx::tma_load_2d(sA, &tmA, &full[stage], a_col, a_row, pol_a);
-          if (meta_now) {
-            const uint8_t* src = p.meta_hw + static_cast<int64_t>(ui.meta_blk0 + kb) * 2048;
-            ptx::bulk_load(sM, src, 2048, &full[stage], pol_a);
+          if constexpr (SPARSE) {
+            for (int mt = 0; mt < ui.subs; ++mt) {
+              const uint8_t* src = p.meta_hw + static_cast<int64_t>(ui.meta_blk0 + mt * ui.nk + kb) * 2048;
+              ptx::bulk_load(sM + mt * 2048, src, 2048, &full[stage], pol_a);
+            }
           }
           if constexpr (!GATHER) {
+            if constexpr (CS == 1) {
 #pragma unroll
-            for (int bx = 0; bx < C::B_BOXES; ++bx)
-              ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS,
-                               kb * C::BK, pol_b);
+              for (int bx = 0; bx < C::B_BOXES; ++bx)
+                ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS,
+                                 kb * C::BK, pol_b);
+            } else {
+              const int32_t r0 = static_cast<int32_t>(crank) * C::B_SLICE_ROWS;
+#pragma unroll
+              for (int bx = 0; bx < C::B_BOXES; ++bx)
+                ptx::tma_load_2d_multicast(sB + bx * C::B_BOX_BYTES + r0 * 128, &tmB, &full[stage],
+                                           ui.n0 + bx * C::B_BOX_COLS, kb * C::BK + r0, kMask, pol_b);
+            }
           }
         }
         if constexpr (GATHER) {
           __syncwarp();
           // lanes 0..15 gather four X rows each (positions past L read row 0; the
-          // packed A is zero there)
+          // packed A is zero there); the row indices were fetched kIdxAhead stages
+          // earlier, so their load latency hides behind the pipeline
           if (lane < C::BK / 4) {
-            int32_t rr[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int32_t j = kb * C::BK + 4 * static_cast<int32_t>(lane) + q;
-              rr[q] = (j < ui.L) ? __ldg(p.indices + ui.idx_base + j) : 0;
-            }
 #pragma unroll
             for (int bx = 0; bx < C::B_BOXES; ++bx)
               ptx::tma_gather4(sB + bx * C::B_BOX_BYTES + 4 * lane * 128, &tmB, &full[stage],
-                               ui.n0 + bx * C::B_BOX_COLS, rr[0], rr[1], rr[2], rr[3], pol_b);
+                               ui.n0 + bx * C::B_BOX_COLS, idx_ring[0][0], idx_ring[0][1], idx_ring[0][2],
+                               idx_ring[0][3], pol_b);
+#pragma unroll
+            for (int d = 0; d + 1 < kIdxAhead; ++d)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) idx_ring[d][q] = idx_ring[d + 1][q];
+            load_idx(ui, kb + kIdxAhead, idx_ring[kIdxAhead - 1]);
           }
         }
         __syncwarp();
         ++issued;
         if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (ok && lane == 0) {
+      // Tail: every stage this CTA filled has been released by all consumers of
+      // the cluster, so no remote arrival or multicast write is still due here.
+      int s = stage;
+      uint32_t ph = phase;
+      const int pending = issued < C::STAGES ? issued : C::STAGES;
+      for (int n = 0; n < pending; ++n) {
+        if (--s < 0) { s = C::STAGES - 1; ph ^= 1u; }
+        wait_bounded(&empty[s], ph, p.err);
       }
     }
     // On abort, wait (bounded) for the copies still in flight before exiting.
@@ -245,13 +316,13 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t acc_phase = 0;
     int meta_slot = 0;
     bool ok = true;
-    for (int32_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const UnitInfo ui = decode_unit<C, GATHER>(p, u);
+    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
       if (lane == 0) ok = wait_bounded(&acc_empty[acc], acc_phase ^ 1u, p.err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || *abort_flag) { *abort_flag = 1; ok = false; break; }
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
       uint32_t cur_meta = 0;
       for (int32_t kb = 0; kb < ui.nk; ++kb) {
         if (lane == 0) ok = wait_bounded(&full[stage], phase, p.err);
@@ -263,34 +334,43 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t sB = sA + C::A_BYTES;
           if constexpr (SPARSE) {
             const uint32_t sM = sB + C::B_BYTES;
-            cur_meta = tmem_base + C::META_COL0 + 4u * static_cast<uint32_t>(meta_slot);
+            cur_meta = tmem_base + C::META_COL0 + static_cast<uint32_t>(C::META_SLOT_COLS * meta_slot);
             meta_slot = (meta_slot + 1) % C::META_SLOTS;
-            // 128 rows x 16 B, rows contiguous: 8-row core matrices 128 B apart
-            ptx::tmem_cp_128x128b(cur_meta, ptx::sdesc(sM, 128, 128, 0));
+            // per sub-tile: 128 rows x 16 B, rows contiguous (8-row core matrices 128 B apart)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              ptx::tmem_cp_128x128b(cur_meta + 4u * mt, ptx::sdesc(sM + 2048u * mt, 128, 128, 0));
           }
 #pragma unroll
-          for (int j = 0; j < C::MMAS; ++j) {
+          for (int j = 0; j < C::MMAS; ++j)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
             const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
             const uint64_t bdesc = ptx::sdesc(sB + j * C::MMA_K * 128, C::B_BOX_BYTES, 1024, 2);
+            const uint32_t d_sub = d_tmem + static_cast<uint32_t>(mt * BN);
+            const uint32_t a_sub = sA + static_cast<uint32_t>(mt * C::A_SUB_BYTES);
             if constexpr (SPARSE) {
-              const uint64_t adesc = ptx::sdesc(sA + j * 32, 16, 512, 4);
+              const uint64_t adesc = ptx::sdesc(a_sub + j * 32, 16, 512, 4);
               // the metadata of instruction j starts at column 2 j of the stage's four
               // (the sparse MMA reads it from an even column: one column for a
               // 16-bit K = 32 step, two for an e4m3 K = 64 step)
-              const uint32_t col = 2u * j;
+              const uint32_t col = 4u * mt + 2u * j;
               if constexpr (C::F8)
-                ptx::mma_sp_f8(d_tmem, adesc, bdesc, cur_meta + col, C::IDESC, accum);
+                ptx::mma_sp_f8(d_sub, adesc, bdesc, cur_meta + col, C::IDESC, accum);
               else
-                ptx::mma_sp_f16(d_tmem, adesc, bdesc, cur_meta + col, C::IDESC, accum);
+                ptx::mma_sp_f16(d_sub, adesc, bdesc, cur_meta + col, C::IDESC, accum);
             } else {
-              const uint64_t adesc = ptx::sdesc(sA + j * 32, 16, 1024, 2);
+              const uint64_t adesc = ptx::sdesc(a_sub + j * 32, 16, 1024, 2);
               if constexpr (C::F8)
-                ptx::mma_f8(d_tmem, adesc, bdesc, C::IDESC, accum);
+                ptx::mma_f8(d_sub, adesc, bdesc, C::IDESC, accum);
               else
-                ptx::mma_f16(d_tmem, adesc, bdesc, C::IDESC, accum);
+                ptx::mma_f16(d_sub, adesc, bdesc, C::IDESC, accum);
             }
           }
-          ptx::mma_commit(&empty[stage]);
+          if constexpr (CS > 1)
+            ptx::mma_commit_multicast(&empty[stage], kMask);
+          else
+            ptx::mma_commit(&empty[stage]);
         }
         __syncwarp();
         if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -308,23 +388,25 @@ __global__ void __launch_bounds__(256, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const uint32_t q = warp & 3u;
+    const uint32_t q = warp & 3u;                 // TMEM lane quadrant this warp may read
+    const uint32_t mt = (warp - 4u) >> 2;         // sub-tile this warp drains
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int32_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const UnitInfo ui = decode_unit<C, GATHER>(p, u);
+    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
       ok = wait_bounded(&acc_full[acc], acc_phase, p.err);
       if (!ok || *abort_flag) { *abort_flag = 1; break; }
       ptx::tc_fence_after();
-      const int32_t row = ui.m0 + static_cast<int32_t>(32 * q + lane);
-      const bool row_ok = row < p.M;
+      const int32_t row = ui.m0 + static_cast<int32_t>(128 * mt + 32 * q + lane);
+      const bool row_ok = row < p.M && !ui.phantom;
       uint8_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy * 2;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         if (ui.nk > 0) {
-          ptx::tmem_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(acc * BN + 32 * c), r);
+          ptx::tmem_ld_32x32b_x32(
+              tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS + mt * BN + 32 * c), r);
           ptx::tmem_ld_wait();
         } else {
 #pragma unroll
@@ -371,6 +453,7 @@ __global__ void __launch_bounds__(256, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  if constexpr (CS > 1) ptx::cluster_sync();  // no CTA leaves while a peer may still signal it
 }
 
 // ------------------------------------------------------------------ host side
@@ -413,19 +496,19 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1>
 cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  using C = Cfg<DT, SPARSE, GATHER, BN>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT>;
   const int eb = C::EB;
   CUtensorMap tA, tB;
   bool ok;
   if constexpr (!GATHER) {
     if constexpr (SPARSE)
-      ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, 128,
+      ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, C::BM,
                     CU_TENSOR_MAP_SWIZZLE_64B);
     else
-      ok = make_map(&tA, a.A, eb, a.K, a.M, a.lda * eb, 128 / eb, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, 128 / eb, C::BK, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = make_map(&tA, a.A, eb, a.K, a.M, a.lda * eb, 128 / eb, C::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, 128 / eb, C::B_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     // packed operand seen as (packed_rows x 64) dense or (packed_rows x 32) values
     if constexpr (SPARSE)
@@ -439,10 +522,12 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   Params p{};
   p.M = static_cast<int32_t>(a.M);
   p.N = static_cast<int32_t>(a.N);
-  p.MB = static_cast<int32_t>(ceil_div(a.M, 128));
+  p.MB = static_cast<int32_t>(ceil_div(a.M, C::BM));
+  p.MB128 = static_cast<int32_t>(ceil_div(a.M, 128));
   p.NB = static_cast<int32_t>(ceil_div(a.N, BN));
+  p.MG = static_cast<int32_t>(ceil_div(p.MB, CS));
   p.nk = static_cast<int32_t>(ceil_div(a.K, C::BK));
-  p.num_units = GATHER ? static_cast<int32_t>(a.nt) * p.NB : p.MB * p.NB;
+  p.num_units = GATHER ? static_cast<int32_t>(a.nt) * p.NB : p.MG * p.NB;
   p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : 0;
   p.alpha = a.alpha;
   p.meta_hw = a.meta_hw;
@@ -454,30 +539,119 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.err = err;
   if (p.num_units == 0) return cudaSuccess;
 
-  auto kern = k_gemm<DT, SPARSE, GATHER, BN>;
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int grid = std::min(p.num_units, sm_count());
-  kern<<<grid, 256, C::SMEM_BYTES, s>>>(tA, tB, p);
-  return cudaGetLastError();
+  if constexpr (CS == 1) {
+    const int grid = std::min(p.num_units, sm_count());
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, p);
+    return cudaGetLastError();
+  } else {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0)) != cudaSuccess)
+      return e;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    // persistent: as many clusters as can be resident at once, at most one per work item
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count() / CS * CS), 1, 1);
+    int max_clusters = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg)) != cudaSuccess) return e;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    const int clusters = std::min(p.num_units, max_clusters);
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CS), 1, 1);
+    return cudaLaunchKernelEx(&cfg, kern, tA, tB, p);
+  }
+}
+
+int cluster_override() {
+  static int v = [] {
+    const char* e = getenv("SSDNN_CLUSTER");
+    return e ? atoi(e) : 0;
+  }();
+  return v;
+}
+
+template <int DT, bool SPARSE, int BN>
+cudaError_t run_clustered(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
+  // Clusters of CTAs on consecutive 128-row blocks of one N block share its X
+  // panel by multicast (opt-in: SSDNN_CLUSTER=2 or 4; measured no faster than
+  // one CTA per panel on the LLM FFN shapes, where the per-SM fill rate, not L2,
+  // limits the kernel).
+  const int64_t MB = ceil_div(a.M, 128);
+  const int ov = cluster_override();
+  if (ov == 4 && MB >= 4) return run<DT, SPARSE, false, BN, 4>(a, s, err);
+  if (ov == 2 && MB >= 2) return run<DT, SPARSE, false, BN, 2>(a, s, err);
+  return run<DT, SPARSE, false, BN, 1>(a, s, err);
+}
+
+// Tile choice by a fill-rate model: a CTA's time is its stage count times the
+// bytes one stage brings into shared memory, and the kernel's time is the number
+// of waves of CTAs (persistent, one per SM) times that. Candidates are
+// (sub-tiles of 128 rows, N tile).
+struct TileChoice {
+  int mt, bn;
+};
+TileChoice choose_tile(bool sparse, int eb, int64_t M, int64_t N) {
+  const TileChoice dense_c[] = {{1, 128}, {1, 256}, {2, 256}};
+  const TileChoice sp16_c[] = {{1, 128}, {1, 256}, {2, 192}};
+  const TileChoice sp8_c[] = {{1, 128}, {1, 256}, {2, 128}};
+  const TileChoice* cand = !sparse ? dense_c : (eb == 2 ? sp16_c : sp8_c);
+  const int64_t sms = sm_count();
+  TileChoice best = cand[0];
+  double best_cost = 1e300;
+  for (int i = 0; i < 3; ++i) {
+    const TileChoice c = cand[i];
+    const int64_t units = ceil_div(M, 128 * c.mt) * ceil_div(N, c.bn);
+    const int64_t waves = ceil_div(units, sms);
+    const int64_t stage = c.mt * (sparse ? 8192 + 2048 : 16384) + 128 * c.bn;
+    const double cost = static_cast<double>(waves) * static_cast<double>(stage) * (1.0 + 0.02 * c.mt);
+    if (cost < best_cost) { best_cost = cost; best = c; }
+  }
+  return best;
+}
+
+int tile_override() {
+  static int v = [] {
+    const char* e = getenv("SSDNN_TILE");  // "MT*1000 + BN", e.g. 2192
+    return e ? atoi(e) : 0;
+  }();
+  return v;
 }
 
 template <int DT>
 cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  // Narrow N or few 128-row blocks: a 128-wide N tile gives more work units.
-  const int64_t units256 = ceil_div(a.M, 128) * ceil_div(a.N, 256);
-  const bool narrow = (a.N <= 128) || (mode < 2 && units256 < 2 * sm_count());
-  switch (mode) {
-    case 0:
-      return narrow ? run<DT, false, false, 128>(a, s, err) : run<DT, false, false, 256>(a, s, err);
-    case 1:
-      return narrow ? run<DT, true, false, 128>(a, s, err) : run<DT, true, false, 256>(a, s, err);
-    case 2:
-      if constexpr (DT != 2) return narrow ? run<DT, false, true, 128>(a, s, err) : run<DT, false, true, 256>(a, s, err);
-      break;
-    case 3:
-      if constexpr (DT != 2) return narrow ? run<DT, true, true, 128>(a, s, err) : run<DT, true, true, 256>(a, s, err);
-      break;
+  constexpr int EB = Elem<DT>::bytes;
+  if (mode == 0 || mode == 1) {
+    const bool sparse = mode == 1;
+    TileChoice c = choose_tile(sparse, EB, a.M, a.N);
+    if (tile_override()) c = TileChoice{tile_override() / 1000, tile_override() % 1000};
+    if (c.mt == 2) {
+      if (!sparse && c.bn == 256) return run<DT, false, false, 256, 1, 2>(a, s, err);
+      if (sparse && EB == 2 && c.bn == 192) {
+        if constexpr (EB == 2) return run<DT, true, false, 192, 1, 2>(a, s, err);
+      }
+      if (sparse && EB == 1 && c.bn == 128) {
+        if constexpr (EB == 1) return run<DT, true, false, 128, 1, 2>(a, s, err);
+      }
+      return cudaErrorInvalidValue;
+    }
+    if (c.bn == 128)
+      return sparse ? run_clustered<DT, true, 128>(a, s, err) : run_clustered<DT, false, 128>(a, s, err);
+    return sparse ? run_clustered<DT, true, 256>(a, s, err) : run_clustered<DT, false, 256>(a, s, err);
+  }
+  // tile-wise: 128-row tiles follow the pattern's tiles
+  const bool narrow = a.N <= 128 || a.nt * ceil_div(a.N, 256) < 2 * sm_count();
+  if constexpr (DT != 2) {
+    if (mode == 2) return narrow ? run<DT, false, true, 128, 1>(a, s, err) : run<DT, false, true, 256, 1>(a, s, err);
+    if (mode == 3) return narrow ? run<DT, true, true, 128, 1>(a, s, err) : run<DT, true, true, 256, 1>(a, s, err);
   }
   return cudaErrorInvalidValue;
 }

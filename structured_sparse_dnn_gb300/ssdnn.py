@@ -91,13 +91,26 @@ def check_device_error(stream: int | None = None) -> int:
 
 # ---------------------------------------------------------------------- 2:4
 def sp24_sizes(dt: int, M: int, K: int) -> tuple[int, int, int]:
+    """(values, meta, meta_hw) sizes in bytes."""
     v, m, h = _sz(), _sz(), _sz()
     _check(lib.sp24_sizes(dt, M, K, C.byref(v), C.byref(m), C.byref(h)), "sp24_sizes")
     return v.value, m.value, h.value
 
 
-def sp24_prune_compress(W: torch.Tensor, canonical_meta: bool = True):
-    """W (M x K, fp16/bf16/e4m3, CUDA) -> (values M x Kp/2, meta M x Kp/8 or None, meta_hw bytes)."""
+@dataclass
+class Sp24:
+    """A 2:4-compressed weight on the device: the values (M x Kp/2), the canonical
+    metadata (optional) and the metadata in the tensor-core operand order."""
+    dt: int
+    M: int
+    K: int
+    values: torch.Tensor
+    meta: torch.Tensor | None
+    meta_hw: torch.Tensor
+
+
+def sp24_prune_compress(W: torch.Tensor, canonical_meta: bool = True) -> Sp24:
+    """W (M x K, fp16/bf16/e4m3, CUDA) -> its 2:4-compressed form."""
     dt = _DT[W.dtype]
     M, K = W.shape
     assert W.stride(1) == 1
@@ -105,23 +118,23 @@ def sp24_prune_compress(W: torch.Tensor, canonical_meta: bool = True):
     Kp = (K + 31) // 32 * 32
     values = torch.empty((M, Kp // 2), dtype=W.dtype, device=W.device)
     meta = torch.empty((M, Kp // 8), dtype=torch.uint8, device=W.device) if canonical_meta else None
-    meta_hw = torch.empty(hb, dtype=torch.uint8, device=W.device)
+    meta_hw = torch.empty(max(16, hb), dtype=torch.uint8, device=W.device)
     _check(lib.sp24_prune_compress(dt, _p(W), M, K, W.stride(0), _p(values), _p(meta), _p(meta_hw),
                                    _stream(W.device)), "sp24_prune_compress")
-    return values, meta, meta_hw
+    return Sp24(dt, M, K, values, meta, meta_hw[:hb])
 
 
-def sp24_gemm(values: torch.Tensor, meta_hw: torch.Tensor, X: torch.Tensor, K: int,
-              out_dtype: torch.dtype | None = None, alpha: float = 1.0, out: torch.Tensor | None = None):
-    """Y = alpha * decompress(values, meta_hw) . X  (M x N)."""
+def sp24_gemm(form: Sp24, X: torch.Tensor, out_dtype: torch.dtype | None = None, alpha: float = 1.0,
+              out: torch.Tensor | None = None):
+    """Y = alpha * decompress(form) . X  (M x N)."""
     dt = _DT[X.dtype]
-    M = values.shape[0]
+    assert dt == form.dt and X.shape[0] == form.K
     N = X.shape[1]
     out_dtype = out_dtype or (torch.bfloat16 if dt == E4M3 else X.dtype)
     if out is None:
-        out = torch.empty((M, N), dtype=out_dtype, device=X.device)
-    _check(lib.sp24_gemm(dt, _DT[out.dtype], M, N, K, _p(values), _p(meta_hw), _p(X), X.stride(0), _p(out),
-                         out.stride(0), alpha, _stream(X.device)), "sp24_gemm")
+        out = torch.empty((form.M, N), dtype=out_dtype, device=X.device)
+    _check(lib.sp24_gemm(dt, _DT[out.dtype], form.M, N, form.K, _p(form.values), _p(form.meta_hw), _p(X),
+                         X.stride(0), _p(out), out.stride(0), alpha, _stream(X.device)), "sp24_gemm")
     return out
 
 

@@ -20,12 +20,12 @@ def test_compress_bit_exact(dt, shape):
     ss = lib()
     M, K = shape
     W = rand_bits(100 + M + K, shape, dt, 0.02 if dt != "f16" else 1.0)
-    values, meta, meta_hw = ss.sp24_prune_compress(dev_tensor(W, dt))
+    f = ss.sp24_prune_compress(dev_tensor(W, dt))
     torch.cuda.synchronize()
     v_ref, m_ref = oracle.sp24.compress(W, dt)
-    assert np.array_equal(bits_of(values), v_ref)
-    assert np.array_equal(bits_of(meta), m_ref)
-    assert np.array_equal(bits_of(meta_hw), oracle.sp24.meta_hw_from_canonical(m_ref, M, K, dt))
+    assert np.array_equal(bits_of(f.values), v_ref)
+    assert np.array_equal(bits_of(f.meta), m_ref)
+    assert np.array_equal(bits_of(f.meta_hw), oracle.sp24.meta_hw_from_canonical(m_ref, M, K, dt))
     assert ss.check_device_error() == 0
 
 
@@ -34,9 +34,9 @@ def test_compress_strided_input():
     M, K, ld = 70, 200, 264
     big = rand_bits(5, (M, ld), "bf16")
     Wt = dev_tensor(big, "bf16")[:, :K]
-    values, meta, meta_hw = ss.sp24_prune_compress(Wt)
+    f = ss.sp24_prune_compress(Wt)
     v_ref, m_ref = oracle.sp24.compress(np.ascontiguousarray(big[:, :K]), "bf16")
-    assert np.array_equal(bits_of(values), v_ref) and np.array_equal(bits_of(meta), m_ref)
+    assert np.array_equal(bits_of(f.values), v_ref) and np.array_equal(bits_of(f.meta), m_ref)
 
 
 @pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
@@ -52,13 +52,15 @@ def test_compress_edge_values(dt):
     W = pool[rng.integers(0, len(pool), size=(96, 512))]
     W[0, :] = pool[6]                       # all-equal groups
     W[1, :] = 0                             # all-zero groups
-    values, meta, meta_hw = ss.sp24_prune_compress(dev_tensor(W, dt))
+    f = ss.sp24_prune_compress(dev_tensor(W, dt))
     v_ref, m_ref = oracle.sp24.compress(W, dt)
-    assert np.array_equal(bits_of(values), v_ref)
-    assert np.array_equal(bits_of(meta), m_ref)
+    assert np.array_equal(bits_of(f.values), v_ref)
+    assert np.array_equal(bits_of(f.meta), m_ref)
 
 
-GEMM_SHAPES = [(128, 256, 64), (200, 72, 136), (256, 512, 1024), (300, 40, 8), (64, 1000, 96), (384, 264, 520)]
+# the last shape selects the 256-row tiles (two 128-row sub-tiles per CTA) with a ragged M
+GEMM_SHAPES = [(128, 256, 64), (200, 72, 136), (256, 512, 1024), (300, 40, 8), (64, 1000, 96), (384, 264, 520),
+               (2000, 8192, 256)]
 
 
 def _check_y(Y, Y_ref, B, out_dt, rel):
@@ -82,9 +84,9 @@ def test_sp24_gemm_within_bound(dt, shape):
     X = rand_bits(300 + N, (K, N), dt, 1.0)
     out_dt = "bf16" if dt == "e4m3" else dt
     alpha = 0.75 if dt == "e4m3" else 1.0
-    values, meta, meta_hw = ss.sp24_prune_compress(dev_tensor(W, dt))
+    f = ss.sp24_prune_compress(dev_tensor(W, dt), canonical_meta=False)
     Y, buf = guarded_output(M, N, torch.bfloat16 if out_dt == "bf16" else torch.float16)
-    ss.sp24_gemm(values, meta_hw, dev_padded(X, dt), K, alpha=alpha, out=Y)
+    ss.sp24_gemm(f, dev_padded(X, dt), alpha=alpha, out=Y)
     torch.cuda.synchronize()
     assert ss.check_device_error() == 0
     v_ref, m_ref = oracle.sp24.compress(W, dt)
@@ -118,8 +120,8 @@ def test_sp24_gemm_identity_is_exact():
     M, K = 256, 256
     W = rand_bits(9, (M, K), "bf16", 1.0)
     X = oracle.codecs.encode(np.eye(K), "bf16")
-    values, _, meta_hw = ss.sp24_prune_compress(dev_tensor(W, "bf16"))
-    Y = ss.sp24_gemm(values, meta_hw, dev_tensor(X, "bf16"), K)
+    f = ss.sp24_prune_compress(dev_tensor(W, "bf16"))
+    Y = ss.sp24_gemm(f, dev_tensor(X, "bf16"))
     assert np.array_equal(bits_of(Y), oracle.sp24.prune(W, "bf16"))
 
 
@@ -127,9 +129,8 @@ def test_k_zero_and_empty():
     ss = lib()
     X = torch.zeros((0, 16), dtype=torch.bfloat16, device="cuda")
     Y = torch.full((8, 16), 3.0, dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros((8, 0), dtype=torch.bfloat16, device="cuda")
-    m = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    ss.sp24_gemm(v, m, X, 0, out=Y)
+    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    ss.sp24_gemm(ss.Sp24(ss.BF16, 8, 0, z, None, z), X, out=Y)
     assert (Y == 0).all()
 
 
@@ -138,8 +139,8 @@ def test_two_calls_in_a_row_agree():
     M, N, K = 256, 256, 512
     W = rand_bits(11, (M, K), "f16")
     X = rand_bits(12, (K, N), "f16")
-    values, _, meta_hw = ss.sp24_prune_compress(dev_tensor(W, "f16"))
+    f = ss.sp24_prune_compress(dev_tensor(W, "f16"))
     Xd = dev_tensor(X, "f16")
-    a = ss.sp24_gemm(values, meta_hw, Xd, K)
-    b = ss.sp24_gemm(values, meta_hw, Xd, K)
+    a = ss.sp24_gemm(f, Xd)
+    b = ss.sp24_gemm(f, Xd)
     assert torch.equal(a, b)

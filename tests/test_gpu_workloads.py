@@ -19,12 +19,11 @@ LARGE = ["llm_ffn_e4m3", "llm_ffn_bf16"]
 def _run_sp24(ss, wl, d):
     Wd = I.torch_view(d["W"], wl.dt).cuda()
     Xd = I.torch_view(d["X"], wl.dt).cuda()
-    values, meta, meta_hw = ss.sp24_prune_compress(Wd)
-    Y = ss.sp24_gemm(values, meta_hw, Xd, wl.K, alpha=d["alpha"],
-                     out_dtype=torch.bfloat16 if wl.out_dt == "bf16" else torch.float16)
+    f = ss.sp24_prune_compress(Wd)
+    Y = ss.sp24_gemm(f, Xd, alpha=d["alpha"], out_dtype=torch.bfloat16 if wl.out_dt == "bf16" else torch.float16)
     torch.cuda.synchronize()
     assert ss.check_device_error() == 0
-    return values, meta, meta_hw, Y, Wd, Xd
+    return f, Y, Wd, Xd
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -32,11 +31,11 @@ def test_small_workload_full(name):
     ss = lib()
     wl = I.WORKLOADS[name]
     d = wl.make()
-    values, meta, meta_hw, Y, _, _ = _run_sp24(ss, wl, d)
+    f, Y, _, _ = _run_sp24(ss, wl, d)
     v_ref, m_ref = oracle.sp24.compress(d["W"], wl.dt)
-    assert np.array_equal(bits_of(values), v_ref)
-    assert np.array_equal(bits_of(meta), m_ref)
-    assert np.array_equal(bits_of(meta_hw), oracle.sp24.meta_hw_from_canonical(m_ref, wl.M, wl.K, wl.dt))
+    assert np.array_equal(bits_of(f.values), v_ref)
+    assert np.array_equal(bits_of(f.meta), m_ref)
+    assert np.array_equal(bits_of(f.meta_hw), oracle.sp24.meta_hw_from_canonical(m_ref, wl.M, wl.K, wl.dt))
     Y_ref = oracle.gemm.gemm_sp24(v_ref, m_ref, wl.K, d["X"], wl.dt, wl.out_dt, d["alpha"])
     B = oracle.gemm.bound(oracle.sp24.decompress(v_ref, m_ref, wl.K), d["X"], wl.dt, d["alpha"])
     ok = oracle.gemm.within_bound(bits_of(Y), Y_ref, B, wl.out_dt, REL[wl.dt])
@@ -53,11 +52,11 @@ def test_large_workload_compress_full_gemm_sampled(name):
     ss = lib()
     wl = I.WORKLOADS[name]
     d = wl.make()
-    values, meta, meta_hw, Y, Wd, Xd = _run_sp24(ss, wl, d)
+    f, Y, Wd, Xd = _run_sp24(ss, wl, d)
     v_ref, m_ref = oracle.sp24.compress(d["W"], wl.dt)
-    assert np.array_equal(bits_of(values), v_ref)
-    assert np.array_equal(bits_of(meta), m_ref)
-    assert np.array_equal(bits_of(meta_hw), oracle.sp24.meta_hw_from_canonical(m_ref, wl.M, wl.K, wl.dt))
+    assert np.array_equal(bits_of(f.values), v_ref)
+    assert np.array_equal(bits_of(f.meta), m_ref)
+    assert np.array_equal(bits_of(f.meta_hw), oracle.sp24.meta_hw_from_canonical(m_ref, wl.M, wl.K, wl.dt))
     rows = _sample_rows(wl.M)
     Yr = bits_of(Y[torch.from_numpy(rows).cuda()])
     Y_ref = oracle.gemm.gemm_sp24(v_ref, m_ref, wl.K, d["X"], wl.dt, wl.out_dt, d["alpha"], rows=rows)
