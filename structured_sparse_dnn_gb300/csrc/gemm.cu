@@ -51,9 +51,11 @@ struct Params {
   int32_t MB, NB;           // BM-row blocks (BM = 128 MT), BN-column blocks
   int32_t MB128;            // 128-row blocks (the metadata's row blocks)
   int32_t MG;               // groups of CS consecutive BM-row blocks (one group per cluster pass)
+  int32_t GR;               // rasterisation: M groups per band; work sweeps a band's N blocks
   int32_t num_units;        // work items: (M group, N block) pairs, or (schedule entry, N block)
   int32_t nk;               // k stages per unit (dense / sp24)
   int32_t out_dt;           // 0 f16, 1 bf16
+  int32_t nstages;          // stages of the shared-memory ring in use (<= the compiled count)
   float alpha;
   const uint8_t* meta_hw;
   const int32_t* schedule;  // TW/TVW: (t, L, P, Q) per tile, in work order
@@ -117,7 +119,12 @@ template <typename C, bool GATHER>
 __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint32_t crank) {
   UnitInfo ui;
   if constexpr (!GATHER) {
-    const int32_t mg = u % p.MG, nb = u / p.MG;
+    // Bands of GR M groups: inside a band the M index runs fastest, then N, so the
+    // CTAs in flight share a few weight rows and a few X panels and both stay in
+    // L2 (plain M-fastest order streams all of W once per wave of N blocks).
+    const int32_t band = u / (p.GR * p.NB), r = u - band * (p.GR * p.NB);
+    const int32_t gh = min(p.GR, p.MG - band * p.GR);
+    const int32_t nb = r / gh, mg = band * p.GR + (r - nb * gh);
     const int32_t mb = mg * C::CLUSTER + static_cast<int32_t>(crank);
     ui.phantom = mb >= p.MB;
     ui.m0 = mb * C::BM;
@@ -284,7 +291,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
         }
         __syncwarp();
         ++issued;
-        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == p.nstages) { stage = 0; phase ^= 1u; }
       }
     }
     if (ok && lane == 0) {
@@ -292,9 +299,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
       // the cluster, so no remote arrival or multicast write is still due here.
       int s = stage;
       uint32_t ph = phase;
-      const int pending = issued < C::STAGES ? issued : C::STAGES;
+      const int pending = issued < p.nstages ? issued : p.nstages;
       for (int n = 0; n < pending; ++n) {
-        if (--s < 0) { s = C::STAGES - 1; ph ^= 1u; }
+        if (--s < 0) { s = p.nstages - 1; ph ^= 1u; }
         wait_bounded(&empty[s], ph, p.err);
       }
     }
@@ -302,9 +309,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
     if (!ok && lane == 0) {
       int s = stage;
       uint32_t ph = phase;
-      const int pending = issued < C::STAGES ? issued : C::STAGES;
+      const int pending = issued < p.nstages ? issued : p.nstages;
       for (int n = 0; n < pending; ++n) {
-        if (--s < 0) { s = C::STAGES - 1; ph ^= 1u; }
+        if (--s < 0) { s = p.nstages - 1; ph ^= 1u; }
         wait_bounded(&full[s], ph, nullptr);
       }
     }
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
             ptx::mma_commit(&empty[stage]);
         }
         __syncwarp();
-        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == p.nstages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
       if (lane == 0) ptx::mma_commit(&acc_full[acc]);
@@ -390,6 +397,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp & 3u;                 // TMEM lane quadrant this warp may read
     const uint32_t mt = (warp - 4u) >> 2;         // sub-tile this warp drains
+    const uint64_t pol_y = ptx::policy_evict_first();  // the output is not re-read here
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -435,8 +443,8 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
         if (n0 + 32 <= p.N) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            reinterpret_cast<uint4*>(dst)[v] =
-                make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+            ptx::st_global_v4_hint(reinterpret_cast<uint4*>(dst) + v, packed[4 * v], packed[4 * v + 1],
+                                   packed[4 * v + 2], packed[4 * v + 3], pol_y);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -526,9 +534,19 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.MB128 = static_cast<int32_t>(ceil_div(a.M, 128));
   p.NB = static_cast<int32_t>(ceil_div(a.N, BN));
   p.MG = static_cast<int32_t>(ceil_div(p.MB, CS));
+  {
+    // bands of at most ~32 M groups, balanced
+    const int64_t bands = ceil_div(p.MG, 32);
+    p.GR = static_cast<int32_t>(ceil_div(p.MG, bands));
+  }
   p.nk = static_cast<int32_t>(ceil_div(a.K, C::BK));
   p.num_units = GATHER ? static_cast<int32_t>(a.nt) * p.NB : p.MG * p.NB;
   p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : 0;
+  p.nstages = C::STAGES;
+  if (const char* e = getenv("SSDNN_STAGES")) {  // tuning: a shorter ring than shared memory allows
+    const int v = atoi(e);
+    if (v >= 2 && v < C::STAGES) p.nstages = v;
+  }
   p.alpha = a.alpha;
   p.meta_hw = a.meta_hw;
   p.schedule = a.schedule;
