@@ -61,6 +61,8 @@ struct Params {
   const int32_t* schedule;  // TW/TVW: (t, L, P, Q) per tile, in work order
   const int32_t* offsets;
   const int32_t* indices;
+  const void* X;            // TW/TVW: the activations, gathered row by row
+  int64_t ldx;              // elements
   uint8_t* Y;
   int64_t ldy;              // elements
   uint32_t* err;
@@ -71,7 +73,17 @@ struct Cfg {
   static constexpr int CLUSTER = CS;                        // CTAs sharing one X panel by multicast
   static constexpr int SUB = MT;                            // 128-row sub-tiles per CTA tile
   static constexpr int BM = 128 * MT;
-  static constexpr int THREADS = 128 + 128 * MT;            // 4 control warps + 4 epilogue warps per sub-tile
+  // 4 control warps, 4 epilogue warps per sub-tile, and for TW/TVW 4 warps that
+  // gather the kept X rows with 16-byte cp.async
+  static constexpr int GATHER_THREADS = GATHER ? 128 : 0;
+  static constexpr int EPI_WARP0 = 4;
+  static constexpr int GATHER_WARP0 = 4 + 4 * MT;
+  static constexpr int THREADS = 128 + 128 * MT + GATHER_THREADS;
+  static constexpr int STAGES_FOR_LAG = ((220 * 1024) / (MT * (SPARSE ? 128 * 64 : 128 * 128) + 128 * BN +
+                                                           (SPARSE ? 2048 * MT : 0)));
+  // stages a gather thread keeps in flight before it must see its oldest copies land
+  // (a larger lag keeps more copies in flight but fewer landed stages ready for the MMA)
+  static constexpr int GATHER_LAG = STAGES_FOR_LAG >= 8 ? 2 : 1;
   static constexpr int EB = Elem<DT>::bytes;
   static constexpr bool F8 = Elem<DT>::f8;
   static constexpr int BK = 128 / EB;                       // dense K per stage
@@ -182,7 +194,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], 1 + C::GATHER_THREADS);
       ptx::mbar_init(&empty[s], CS);
     }
     for (int a = 0; a < C::NACC; ++a) {
@@ -217,24 +229,8 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
     uint32_t phase = 0;
     int issued = 0;
     bool ok = true;
-    // TW/TVW: ring of the X row indices of the next kIdxAhead stages (lanes 0..15)
-    constexpr int kIdxAhead = 4;
-    int32_t idx_ring[kIdxAhead][4];
-    auto load_idx = [&](const UnitInfo& ui, int32_t kb, int32_t (&r)[4]) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int32_t j = kb * C::BK + 4 * static_cast<int32_t>(lane) + q;
-        r[q] = (kb < ui.nk && j < ui.L) ? __ldg(p.indices + ui.idx_base + j) : 0;
-      }
-    };
     for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
       const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
-      if constexpr (GATHER) {
-        if (lane < C::BK / 4) {
-#pragma unroll
-          for (int d = 0; d < kIdxAhead; ++d) load_idx(ui, d, idx_ring[d]);
-        }
-      }
       for (int32_t kb = 0; kb < ui.nk; ++kb) {
         if (*abort_flag) { ok = false; break; }
         if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, p.err);
@@ -244,7 +240,8 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
         uint8_t* sB = sA + C::A_BYTES;
         uint8_t* sM = sB + C::B_BYTES;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES + (SPARSE ? 2048 * ui.subs : 0));
+          ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0 : C::B_BYTES) +
+                                                       (SPARSE ? 2048 * ui.subs : 0));
           // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
           // rows past M read as zeros
           const int32_t a_col = GATHER ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
@@ -269,24 +266,6 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
                 ptx::tma_load_2d_multicast(sB + bx * C::B_BOX_BYTES + r0 * 128, &tmB, &full[stage],
                                            ui.n0 + bx * C::B_BOX_COLS, kb * C::BK + r0, kMask, pol_b);
             }
-          }
-        }
-        if constexpr (GATHER) {
-          __syncwarp();
-          // lanes 0..15 gather four X rows each (positions past L read row 0; the
-          // packed A is zero there); the row indices were fetched kIdxAhead stages
-          // earlier, so their load latency hides behind the pipeline
-          if (lane < C::BK / 4) {
-#pragma unroll
-            for (int bx = 0; bx < C::B_BOXES; ++bx)
-              ptx::tma_gather4(sB + bx * C::B_BOX_BYTES + 4 * lane * 128, &tmB, &full[stage],
-                               ui.n0 + bx * C::B_BOX_COLS, idx_ring[0][0], idx_ring[0][1], idx_ring[0][2],
-                               idx_ring[0][3], pol_b);
-#pragma unroll
-            for (int d = 0; d + 1 < kIdxAhead; ++d)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) idx_ring[d][q] = idx_ring[d + 1][q];
-            load_idx(ui, kb + kIdxAhead, idx_ring[kIdxAhead - 1]);
           }
         }
         __syncwarp();
@@ -393,7 +372,75 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
       wait_bounded(drain, 0, nullptr);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (GATHER && warp >= C::GATHER_WARP0) {
+    // ------------------------------------------------------------ X-row gather (TW/TVW)
+    // Gather warp w copies stage rows r = 4 i + w (i < 16). Lanes take consecutive
+    // 16-byte chunks of a row (a warp instruction copies 512 contiguous bytes of X:
+    // one row for a 256-wide N tile, two rows for 128), straight into the
+    // 128B-swizzled MN-major operand layout; rows past L_t and columns past N are
+    // zero-filled. A thread arrives on a stage's full barrier GATHER_LAG stages
+    // later, after waiting for its own copies of that stage and fencing them for
+    // the tensor core's async proxy.
+    const int w = warp - C::GATHER_WARP0;
+    constexpr int CPR = BN / 8;                      // 16-byte chunks per row
+    constexpr int RPI = 32 / CPR;                    // rows per warp instruction
+    constexpr int ITERS = 16 / RPI;                  // instructions per stage
+    const int sub = static_cast<int>(lane) / CPR, q = static_cast<int>(lane) % CPR;
+    const int col = 8 * q;                           // column within the N tile
+    const int bx = col >> 6, cc = (col & 63) >> 3;   // 64-column box, 16-byte chunk in its row
+    constexpr int kIdxAhead = 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    int lag_stage[C::GATHER_LAG + 1];
+    int pending = 0;
+    bool ok = true;
+    const uint16_t* X = static_cast<const uint16_t*>(p.X);
+    int32_t idx_ring[kIdxAhead];                     // lane l < 16: X row of stage row 4 l + w
+    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
+      const int32_t gcol = ui.n0 + col;
+      const uint32_t col_bytes = gcol >= p.N ? 0u : static_cast<uint32_t>(min(8, p.N - gcol) * 2);
+      auto row_of = [&](int32_t kb) -> int32_t {
+        const int32_t j = kb * C::BK + 4 * static_cast<int32_t>(lane) + w;
+        return (lane < 16 && kb < ui.nk && j < ui.L) ? __ldg(p.indices + ui.idx_base + j) : -1;
+      };
+#pragma unroll
+      for (int d = 0; d < kIdxAhead; ++d) idx_ring[d] = row_of(d);
+      for (int32_t kb = 0; kb < ui.nk; ++kb) {
+        if (*abort_flag) { ok = false; break; }
+        if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, p.err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) { *abort_flag = 1; break; }
+        uint8_t* sB = smem + stage * C::STAGE_BYTES + C::A_BYTES;
+#pragma unroll
+        for (int i = 0; i < ITERS; ++i) {
+          const int ri = i * RPI + sub;              // warp-local row 0..15
+          const int r = 4 * ri + w;                  // stage row 0..63
+          const int32_t xrow = __shfl_sync(0xffffffffu, idx_ring[0], ri);
+          const uint32_t bytes = xrow < 0 ? 0u : col_bytes;
+          const uint16_t* src = bytes ? X + static_cast<int64_t>(xrow) * p.ldx + gcol : X;
+          ptx::cp_async_16(sB + bx * C::B_BOX_BYTES + r * 128 + ((cc ^ (r & 7)) << 4), src, bytes);
+        }
+        ptx::cp_async_commit();
+#pragma unroll
+        for (int d = 0; d + 1 < kIdxAhead; ++d) idx_ring[d] = idx_ring[d + 1];
+        idx_ring[kIdxAhead - 1] = row_of(kb + kIdxAhead);
+        lag_stage[pending++] = stage;
+        if (pending > C::GATHER_LAG) {
+          ptx::cp_async_wait<C::GATHER_LAG>();
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(&full[lag_stage[0]]);
+#pragma unroll
+          for (int d = 0; d < C::GATHER_LAG; ++d) lag_stage[d] = lag_stage[d + 1];
+          --pending;
+        }
+        if (++stage == p.nstages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    for (int d = 0; d < pending; ++d) ptx::mbar_arrive(&full[lag_stage[d]]);
+  } else if (warp >= C::EPI_WARP0 && warp < C::EPI_WARP0 + 4 * MT) {
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp & 3u;                 // TMEM lane quadrant this warp may read
     const uint32_t mt = (warp - 4u) >> 2;         // sub-tile this warp drains
@@ -552,6 +599,8 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.schedule = a.schedule;
   p.offsets = a.offsets;
   p.indices = a.indices;
+  p.X = a.X;
+  p.ldx = a.ldx;
   p.Y = static_cast<uint8_t*>(a.Y);
   p.ldy = a.ldy;
   p.err = err;
@@ -620,7 +669,8 @@ struct TileChoice {
 TileChoice choose_tile(bool sparse, int eb, int64_t M, int64_t N) {
   const TileChoice dense_c[] = {{1, 128}, {1, 256}, {2, 256}};
   const TileChoice sp16_c[] = {{1, 128}, {1, 256}, {2, 192}};
-  const TileChoice sp8_c[] = {{1, 128}, {1, 256}, {2, 128}};
+  // e4m3 2:4: the 256x128 tile measured slower than 128x256 on the LLM FFN shape
+  const TileChoice sp8_c[] = {{1, 128}, {1, 256}, {1, 256}};
   const TileChoice* cand = !sparse ? dense_c : (eb == 2 ? sp16_c : sp8_c);
   const int64_t sms = sm_count();
   TileChoice best = cand[0];
@@ -666,7 +716,8 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
     return sparse ? run_clustered<DT, true, 256>(a, s, err) : run_clustered<DT, false, 256>(a, s, err);
   }
   // tile-wise: 128-row tiles follow the pattern's tiles
-  const bool narrow = a.N <= 128 || a.nt * ceil_div(a.N, 256) < 2 * sm_count();
+  bool narrow = a.N <= 128 || a.nt * ceil_div(a.N, 256) < 2 * sm_count();
+  if (const char* e = getenv("SSDNN_GATHER_BN")) narrow = atoi(e) == 128;  // tuning
   if constexpr (DT != 2) {
     if (mode == 2) return narrow ? run<DT, false, true, 128, 1>(a, s, err) : run<DT, false, true, 256, 1>(a, s, err);
     if (mode == 3) return narrow ? run<DT, true, true, 128, 1>(a, s, err) : run<DT, true, true, 256, 1>(a, s, err);
