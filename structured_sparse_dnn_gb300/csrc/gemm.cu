@@ -68,7 +68,7 @@ struct Params {
   uint32_t* err;
 };
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128>
 struct Cfg {
   static constexpr int CLUSTER = CS;                        // CTAs sharing one X panel by multicast
   static constexpr int SUB = MT;                            // 128-row sub-tiles per CTA tile
@@ -96,9 +96,15 @@ struct Cfg {
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int MMA_K = (SPARSE ? 64 : 32) / EB;      // dense K per instruction
   static constexpr int MMAS = BK / MMA_K;                    // instructions per stage
-  static constexpr int B_BOX_COLS = 128 / EB;                // columns per 128-byte B box
+  // B boxes are BK rows of BROW bytes (128: 128B swizzle; 64: 64B swizzle, which
+  // lets an e4m3 N tile be a multiple of 64 columns)
+  static constexpr int B_ROW = BROW;
+  static constexpr int B_BOX_COLS = BROW / EB;               // columns per B box
   static constexpr int B_BOXES = BN / B_BOX_COLS;
-  static constexpr int B_BOX_BYTES = BK * 128;
+  static constexpr int B_BOX_BYTES = BK * BROW;
+  static constexpr int B_SBO = 8 * BROW;                     // 8-row swizzle atom
+  static constexpr uint32_t B_SWZ = BROW == 128 ? 2u : 4u;
+  static_assert(BROW == 128 || (BROW == 64 && !GATHER), "the gather writes 128-byte rows");
   static constexpr int ACC_COLS = MT * BN;                  // fp32 accumulator columns of one tile
   static constexpr int META_SLOTS = 4;
   static constexpr int META_SLOT_COLS = 4 * MT;             // one 128x128b copy per sub-tile
@@ -109,7 +115,7 @@ struct Cfg {
   static constexpr uint32_t IDESC = ptx::idesc(Elem<DT>::mma_fmt, Elem<DT>::mma_fmt, SPARSE, 128, BN,
                                                false, true);
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-  static_assert(B_BOXES * B_BOX_COLS == BN, "BN must be a multiple of the 128-byte box width");
+  static_assert(B_BOXES * B_BOX_COLS == BN, "BN must be a multiple of the B box width");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
   static_assert(MT == 1 || (CS == 1 && !GATHER), "256-row tiles: no cluster, no gather");
   static_assert(CS == 1 || !GATHER, "gathered B rows differ per tile: no multicast");
@@ -165,10 +171,10 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
   return ui;
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT>
-__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 1)
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW>
+__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>;
   // Clusters of CS CTAs along M share each X panel: CTA rank r loads rows
   // [r BK/CS, (r+1) BK/CS) of every B box of a stage and multicasts them to the
   // whole cluster, so a stage is complete only when all CS slices have landed and
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
               const int32_t r0 = static_cast<int32_t>(crank) * C::B_SLICE_ROWS;
 #pragma unroll
               for (int bx = 0; bx < C::B_BOXES; ++bx)
-                ptx::tma_load_2d_multicast(sB + bx * C::B_BOX_BYTES + r0 * 128, &tmB, &full[stage],
+                ptx::tma_load_2d_multicast(sB + bx * C::B_BOX_BYTES + r0 * C::B_ROW, &tmB, &full[stage],
                                            ui.n0 + bx * C::B_BOX_COLS, kb * C::BK + r0, kMask, pol_b);
             }
           }
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT>::THREADS, 
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
-            const uint64_t bdesc = ptx::sdesc(sB + j * C::MMA_K * 128, C::B_BOX_BYTES, 1024, 2);
+            const uint64_t bdesc = ptx::sdesc(sB + j * C::MMA_K * C::B_ROW, C::B_BOX_BYTES, C::B_SBO, C::B_SWZ);
             const uint32_t d_sub = d_tmem + static_cast<uint32_t>(mt * BN);
             const uint32_t a_sub = sA + static_cast<uint32_t>(mt * C::A_SUB_BYTES);
             if constexpr (SPARSE) {
@@ -551,9 +557,9 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128>
 cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>;
   const int eb = C::EB;
   CUtensorMap tA, tB;
   bool ok;
@@ -563,7 +569,8 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
                     CU_TENSOR_MAP_SWIZZLE_64B);
     else
       ok = make_map(&tA, a.A, eb, a.K, a.M, a.lda * eb, 128 / eb, C::BM, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, 128 / eb, C::B_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::B_SLICE_ROWS,
+                        BROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
     // packed operand seen as (packed_rows x 64) dense or (packed_rows x 32) values
     if constexpr (SPARSE)
@@ -606,7 +613,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.err = err;
   if (p.num_units == 0) return cudaSuccess;
 
-  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT>;
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if constexpr (CS == 1) {
@@ -669,8 +676,8 @@ struct TileChoice {
 TileChoice choose_tile(bool sparse, int eb, int64_t M, int64_t N) {
   const TileChoice dense_c[] = {{1, 128}, {1, 256}, {2, 256}};
   const TileChoice sp16_c[] = {{1, 128}, {1, 256}, {2, 192}};
-  // e4m3 2:4: the 256x128 tile measured slower than 128x256 on the LLM FFN shape
-  const TileChoice sp8_c[] = {{1, 128}, {1, 256}, {1, 256}};
+  // e4m3 2:4: 256x192 tiles (64-byte B boxes); 256x128 measured slower than 128x256
+  const TileChoice sp8_c[] = {{1, 128}, {1, 256}, {2, 192}};
   const TileChoice* cand = !sparse ? dense_c : (eb == 2 ? sp16_c : sp8_c);
   const int64_t sms = sm_count();
   TileChoice best = cand[0];
@@ -706,8 +713,8 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
       if (sparse && EB == 2 && c.bn == 192) {
         if constexpr (EB == 2) return run<DT, true, false, 192, 1, 2>(a, s, err);
       }
-      if (sparse && EB == 1 && c.bn == 128) {
-        if constexpr (EB == 1) return run<DT, true, false, 128, 1, 2>(a, s, err);
+      if (sparse && EB == 1 && c.bn == 192) {
+        if constexpr (EB == 1) return run<DT, true, false, 192, 1, 2, 64>(a, s, err);
       }
       return cudaErrorInvalidValue;
     }
