@@ -50,6 +50,23 @@ def peaks() -> dict:
     return p
 
 
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the sparse GEMM on this workload from
+    the committed ncu capture, if the kernel source is unchanged since; else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    with open(os.path.join(ROOT, "structured_sparse_dnn_gb300", "csrc", "gemm.cu"), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    ent = tab.get(workload)
+    if not ent or ent.get("gemm_cu_sha256_16") != sha:
+        return None
+    return ent["dram_bytes_per_launch"]
+
+
 def tensor_peak_effective(dt: str, pk: dict, sustained: bool = False) -> float:
     """2:4-sparse tensor peak in effective (nonzero) TFLOP/s: the sparse core runs
     twice the dense-equivalent rate, i.e. one dense peak of nonzero MACs. e4m3 is
@@ -242,7 +259,8 @@ def run_gpu(args) -> None:
             "pct_of_sparse_peak": round(100.0 * achieved / peak_eff, 2),
             "dense_equivalent_tflops": round(2 * achieved, 2),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak_eff, 1),
-                         "unit": "TFLOP/s", "frac": round(achieved / peak_eff, 4), "traffic": None,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak_eff, 4),
+                         "traffic": measured_traffic(wl.name),
                          "peak_note": f"2:4-sparse {wl.dt} peak in nonzero-MAC TFLOP/s = "
                                       f"{'2 x ' if wl.dt == 'e4m3' else ''}{pk['source']} bf16 dense burst "
                                       f"{pk['bf16_tflops']}"},
