@@ -313,6 +313,46 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd) -> dict:
         rows["dense_gemm_bf16"] = {"workload": wb.name, "ms": round(t, 4),
                                    "TFLOP/s": round(2.0 * wb.M * wb.N * wb.K / (t * 1e-3) / 1e12, 1)}
         del db, Wb, Xb, fb, Yb
+    # a2 on the small workloads (toy, BERT FFN up/down, ResNet-50 1x1): one launch
+    # after an L2 flush (events around it), and 20 launches back to back in one
+    # CUDA graph (L2 warm, launch overhead amortised)
+    small = {}
+    for name in ("toy_fp16", "bert_ffn_up_bf16", "bert_ffn_down_bf16", "resnet50_1x1_fp16"):
+        ws = I.WORKLOADS[name]
+        dsm, Ws, Xs, fs = make_sp24(ws, dev, ss)
+        Ys = torch.empty((ws.M, ws.N), dtype=Ws.dtype, device=dev)
+        t_cold = statistics.median(timed_steps(lambda: ss.sp24_gemm(fs, Xs, out=Ys), steps, 3, flush, stream))
+        t_dense = statistics.median(timed_steps(lambda: ss.dense_gemm(Ws, Xs, out=Ys), steps, 3, flush, stream))
+        reps = 20
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            ss.sp24_gemm(fs, Xs, out=Ys)          # first call outside capture (library set-up)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+                for _ in range(reps):
+                    ss.sp24_gemm(fs, Xs, out=Ys)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(side)
+        with torch.cuda.stream(side):
+            for _ in range(5):
+                g.replay()
+        b.record(side)
+        torch.cuda.synchronize()
+        t_warm = a.elapsed_time(b) / (5 * reps)
+        vb_s, _, hb_s = ss.sp24_sizes(ss._DT[Ws.dtype], ws.M, ws.K)
+        nbytes = vb_s + hb_s + ws.K * ws.N * 2 + ws.M * ws.N * 2
+        small[name] = {"MxNxK": f"{ws.M}x{ws.N}x{ws.K}", "us_l2_flushed": round(t_cold * 1e3, 2),
+                       "dense_us_l2_flushed": round(t_dense * 1e3, 2),
+                       "us_graph_back_to_back": round(t_warm * 1e3, 2),
+                       "effective_TFLOP/s_graph": round(ws.M * ws.N * ws.K / (t_warm * 1e-3) / 1e12, 1),
+                       "GB/s_graph": round(nbytes / (t_warm * 1e-3) / 1e9, 1)}
+        del dsm, Ws, Xs, fs, Ys, g
+    rows["sp24_gemm_small_configs"] = small
     # a3-a7: tile-wise prune and the TW / TVW gather GEMMs vs the same-kernel dense GEMM
     tw = I.WORKLOADS["tile_wise_4096_bf16"]
     dt_ = tw.make()

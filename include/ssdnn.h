@@ -63,6 +63,17 @@ int ssdnn_version(void);
  * Returns SSDNN_OK, SSDNN_ERR_TIMEOUT or SSDNN_ERR_DEVICE. */
 int ssdnn_check_device_error(void* stream);
 
+/* Failure-detection self-test. Launches one thread on `stream` that waits,
+ * through the same bounded wait the GEMM pipeline uses, on an mbarrier that
+ * nothing arrives on. After `limit_us` microseconds (1 .. 1000000) the wait
+ * gives up, sets the timeout bit of this device's error word and the kernel
+ * returns normally, so the context stays usable; the following
+ * ssdnn_check_device_error() then returns SSDNN_ERR_TIMEOUT. Returns
+ * SSDNN_ERR_INVALID_ARG for a limit outside the range, else the launch status.
+ * No passage of the pages defines this call: it tests the library's own
+ * recovery path (kernels give up on a stalled pipeline instead of hanging). */
+int ssdnn_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
 /* ------------------------------------------------------------------ 2:4 ----
  * Compressed 2:4 layouts (Kp = round_up(K, 32)):
  *   values   M x Kp/2 elements, row-major: the kept values of each group in

@@ -34,6 +34,16 @@ uint32_t* error_word() {
   return g_err_ptr[dev];
 }
 
+// One thread waits on an mbarrier that nothing ever arrives on, with the given
+// limit: the wait must give up, record a timeout in the error word and return.
+__global__ void k_selftest_timeout(uint32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  ptx::mbar_init(&bar, 1);
+  ptx::fence_mbar_init();
+  wait_bounded(&bar, 0, err, limit_ns);
+}
+
 int elem_bytes(int dt) { return dt == SSDNN_E4M3 ? 1 : 2; }
 bool valid_dt(int dt) { return dt == SSDNN_F16 || dt == SSDNN_BF16 || dt == SSDNN_E4M3; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -138,6 +148,14 @@ int ssdnn_check_device_error(void* stream) {
   if (v & kErrTimeout) return SSDNN_ERR_TIMEOUT;
   if (v) return SSDNN_ERR_DEVICE;
   return SSDNN_OK;
+}
+
+int ssdnn_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return SSDNN_ERR_INVALID_ARG;
+  uint32_t* w = error_word();
+  if (!w) return SSDNN_ERR_CUDA;
+  k_selftest_timeout<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(w, uint64_t(limit_us) * 1000ull);
+  return from_cuda(cudaGetLastError());
 }
 
 int sp24_sizes(int dt, int64_t M, int64_t K, size_t* values_bytes, size_t* meta_bytes, size_t* meta_hw_bytes) {

@@ -79,29 +79,15 @@ __global__ void __launch_bounds__(256) k_sp24_compress(const uint8_t* __restrict
       if (k0 + 4 * g + 4 > K) break;  // K % 4 == 0: a group is entirely in or out
       const uint32_t e0 = elem<EB>(w, 4 * g + 0), e1 = elem<EB>(w, 4 * g + 1);
       const uint32_t e2 = elem<EB>(w, 4 * g + 2), e3 = elem<EB>(w, 4 * g + 3);
-      const uint32_t m0 = e0 & kMask, m1 = e1 & kMask, m2 = e2 & kMask, m3 = e3 & kMask;
-      // first kept: lowest position among the largest magnitudes
-      int a = 0;
-      uint32_t ma = m0;
-      if (m1 > ma) { a = 1; ma = m1; }
-      if (m2 > ma) { a = 2; ma = m2; }
-      if (m3 > ma) { a = 3; ma = m3; }
-      // second kept: lowest position among the largest of the other three
-      int b = -1;
-      uint32_t mb = 0;
-      if (a != 0) { b = 0; mb = m0; }
-      if (a != 1 && (b < 0 || m1 > mb)) { b = 1; mb = m1; }
-      if (a != 2 && (b < 0 || m2 > mb)) { b = 2; mb = m2; }
-      if (a != 3 && (b < 0 || m3 > mb)) { b = 3; mb = m3; }
-      const int j0 = a < b ? a : b;
-      const int j1 = a < b ? b : a;
-      const uint32_t v0 = j0 == 0 ? e0 : (j0 == 1 ? e1 : e2);          // j0 <= 2
-      const uint32_t v1 = j1 == 3 ? e3 : (j1 == 2 ? e2 : e1);          // j1 >= 1
-      nib = (nib & ~(0xFu << (4 * g))) | (static_cast<uint32_t>(j0 | (j1 << 2)) << (4 * g));
+      const uint32_t sel = top2_nibble(e0 & kMask, e1 & kMask, e2 & kMask, e3 & kMask);
+      const uint32_t j0 = sel & 3u, j1 = sel >> 2;
+      nib = (nib & ~(0xFu << (4 * g))) | (sel << (4 * g));
+      // gather the two kept values with one byte permute of the group's bytes
       if constexpr (EB == 2) {
-        outv[g] = v0 | (v1 << 16);
+        outv[g] = __byte_perm(w[2 * g], w[2 * g + 1],
+                              (2 * j0) | ((2 * j0 + 1) << 4) | ((2 * j1) << 8) | ((2 * j1 + 1) << 12));
       } else {
-        outv[g >> 1] |= (v0 | (v1 << 8)) << ((g & 1) * 16);
+        outv[g >> 1] |= __byte_perm(w[g], 0u, j0 | (j1 << 4) | 0x4400u) << ((g & 1) * 16);
       }
     }
   }

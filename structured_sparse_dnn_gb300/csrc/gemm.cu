@@ -674,15 +674,18 @@ struct TileChoice {
   int mt, bn;
 };
 TileChoice choose_tile(bool sparse, int eb, int64_t M, int64_t N) {
-  const TileChoice dense_c[] = {{1, 128}, {1, 256}, {2, 256}};
-  const TileChoice sp16_c[] = {{1, 128}, {1, 256}, {2, 192}};
+  // 16-bit inputs also have 128x64 tiles, which give small-M shapes (a BERT FFN
+  // down projection: 768 rows) twice the work units of 128x128
+  const TileChoice dense_c[] = {{1, 64}, {1, 128}, {1, 256}, {2, 256}};
+  const TileChoice sp16_c[] = {{1, 64}, {1, 128}, {1, 256}, {2, 192}};
   // e4m3 2:4: 256x192 tiles (64-byte B boxes); 256x128 measured slower than 128x256
-  const TileChoice sp8_c[] = {{1, 128}, {1, 256}, {2, 192}};
-  const TileChoice* cand = !sparse ? dense_c : (eb == 2 ? sp16_c : sp8_c);
+  const TileChoice sp8_c[] = {{1, 128}, {1, 128}, {1, 256}, {2, 192}};
+  const TileChoice dense8_c[] = {{1, 128}, {1, 128}, {1, 256}, {2, 256}};
+  const TileChoice* cand = !sparse ? (eb == 2 ? dense_c : dense8_c) : (eb == 2 ? sp16_c : sp8_c);
   const int64_t sms = sm_count();
   TileChoice best = cand[0];
   double best_cost = 1e300;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const TileChoice c = cand[i];
     const int64_t units = ceil_div(M, 128 * c.mt) * ceil_div(N, c.bn);
     const int64_t waves = ceil_div(units, sms);
@@ -716,6 +719,11 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
       if (sparse && EB == 1 && c.bn == 192) {
         if constexpr (EB == 1) return run<DT, true, false, 192, 1, 2, 64>(a, s, err);
       }
+      return cudaErrorInvalidValue;
+    }
+    if (c.bn == 64) {
+      if constexpr (EB == 2)
+        return sparse ? run<DT, true, false, 64, 1>(a, s, err) : run<DT, false, false, 64, 1>(a, s, err);
       return cudaErrorInvalidValue;
     }
     if (c.bn == 128)

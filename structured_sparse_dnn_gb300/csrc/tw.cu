@@ -195,24 +195,10 @@ __global__ void __launch_bounds__(512) k_tw_pack(const uint8_t* __restrict__ W, 
       nib = 0x4u;
       if (j < L && row < M) {  // L % 4 == 0: the group is entirely kept
         const uint32_t e0 = wrow[idx[j]], e1 = wrow[idx[j + 1]], e2 = wrow[idx[j + 2]], e3 = wrow[idx[j + 3]];
-        const uint32_t m0 = e0 & 0x7FFFu, m1 = e1 & 0x7FFFu, m2 = e2 & 0x7FFFu, m3 = e3 & 0x7FFFu;
-        int a = 0;
-        uint32_t ma = m0;
-        if (m1 > ma) { a = 1; ma = m1; }
-        if (m2 > ma) { a = 2; ma = m2; }
-        if (m3 > ma) { a = 3; ma = m3; }
-        int b = -1;
-        uint32_t mb = 0;
-        if (a != 0) { b = 0; mb = m0; }
-        if (a != 1 && (b < 0 || m1 > mb)) { b = 1; mb = m1; }
-        if (a != 2 && (b < 0 || m2 > mb)) { b = 2; mb = m2; }
-        if (a != 3 && (b < 0 || m3 > mb)) { b = 3; mb = m3; }
-        const int j0 = a < b ? a : b;
-        const int j1 = a < b ? b : a;
-        const uint32_t v0 = j0 == 0 ? e0 : (j0 == 1 ? e1 : e2);
-        const uint32_t v1 = j1 == 3 ? e3 : (j1 == 2 ? e2 : e1);
-        v01 = v0 | (v1 << 16);
-        nib = static_cast<uint32_t>(j0 | (j1 << 2));
+        nib = top2_nibble(e0 & 0x7FFFu, e1 & 0x7FFFu, e2 & 0x7FFFu, e3 & 0x7FFFu);
+        const uint32_t j0 = nib & 3u, j1 = nib >> 2;
+        v01 = __byte_perm(e0 | (e1 << 16), e2 | (e3 << 16),
+                          (2 * j0) | ((2 * j0 + 1) << 4) | ((2 * j1) << 8) | ((2 * j1 + 1) << 12));
       }
       *reinterpret_cast<uint32_t*>(packed + 64 * P + 4096 * c + 32 * r + 2 * lane) = v01;
     }

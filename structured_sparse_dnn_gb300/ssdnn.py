@@ -30,6 +30,7 @@ _SIGS = {
     "ssdnn_status_str": ([C.c_int], C.c_char_p),
     "ssdnn_version": ([], C.c_int),
     "ssdnn_check_device_error": ([_ptr], C.c_int),
+    "ssdnn_selftest_wait_timeout": ([C.c_uint32, _ptr], C.c_int),
     "sp24_sizes": ([C.c_int, _i64, _i64, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "sp24_prune_compress": ([C.c_int, _ptr, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], C.c_int),
     "sp24_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _i64, _ptr, _i64, C.c_float, _ptr],
@@ -87,6 +88,13 @@ def status_str(status: int) -> str:
 def check_device_error(stream: int | None = None) -> int:
     """Synchronises the stream and returns (and clears) the device error status."""
     return lib.ssdnn_check_device_error(stream if stream is not None else _stream(None))
+
+
+def selftest_wait_timeout(limit_us: int = 1000, stream: int | None = None) -> None:
+    """Launches the bounded-wait self-test: a wait that nothing completes gives up
+    after limit_us and records a timeout; check_device_error() then reports it."""
+    _check(lib.ssdnn_selftest_wait_timeout(limit_us, stream if stream is not None else _stream(None)),
+           "ssdnn_selftest_wait_timeout")
 
 
 # ---------------------------------------------------------------------- 2:4

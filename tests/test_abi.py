@@ -95,3 +95,6 @@ def test_argument_errors_before_any_device_work(ssdnn):
     # empty problems are valid no-ops
     assert lib.sp24_gemm(0, 0, 0, 4, 8, None, None, None, 4, None, 4, 1.0, None) == 0
     assert lib.sp24_prune_compress(0, None, 0, 8, 8, None, None, None, None) == 0
+    # the wait-timeout self-test takes a limit of 1 us .. 1 s
+    assert lib.ssdnn_selftest_wait_timeout(0, None) == 1
+    assert lib.ssdnn_selftest_wait_timeout(1000001, None) == 1

@@ -58,9 +58,12 @@ def test_compress_edge_values(dt):
     assert np.array_equal(bits_of(f.meta), m_ref)
 
 
-# the last shape selects the 256-row tiles (two 128-row sub-tiles per CTA) with a ragged M
+# The tile chooser gives the small shapes 128x64 tiles (16-bit) or 128x128
+# (e4m3); (1280, 1000, 192) takes 128x128 and (3072, 1000, 128) 128x256 tiles,
+# both with a ragged N; the last shape selects the 256-row tiles (two 128-row
+# sub-tiles per CTA) with a ragged M.
 GEMM_SHAPES = [(128, 256, 64), (200, 72, 136), (256, 512, 1024), (300, 40, 8), (64, 1000, 96), (384, 264, 520),
-               (2000, 8192, 256)]
+               (1280, 1000, 192), (3072, 1000, 128), (2000, 8192, 256)]
 
 
 def _check_y(Y, Y_ref, B, out_dt, rel):
@@ -144,3 +147,22 @@ def test_two_calls_in_a_row_agree():
     a = ss.sp24_gemm(f, Xd)
     b = ss.sp24_gemm(f, Xd)
     assert torch.equal(a, b)
+
+
+def test_bounded_wait_reports_timeout_without_fault():
+    """Failure detection on the device: a wait that nothing completes gives up
+    after its limit, the kernel returns, the host reads SSDNN_ERR_TIMEOUT from
+    the error word, and the context keeps working afterwards."""
+    ss = lib()
+    assert ss.check_device_error() == 0
+    ss.selftest_wait_timeout(2000)
+    assert ss.check_device_error() == 4          # SSDNN_ERR_TIMEOUT
+    assert ss.check_device_error() == 0          # the word was cleared
+    # the context is still usable: a GEMM right after runs and is exact
+    M, K = 128, 128
+    W = rand_bits(13, (M, K), "bf16", 1.0)
+    X = oracle.codecs.encode(np.eye(K), "bf16")
+    f = ss.sp24_prune_compress(dev_tensor(W, "bf16"))
+    Y = ss.sp24_gemm(f, dev_tensor(X, "bf16"))
+    assert np.array_equal(bits_of(Y), oracle.sp24.prune(W, "bf16"))
+    assert ss.check_device_error() == 0
