@@ -167,6 +167,32 @@ def timed_steps(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> lis
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def mma_microbench(ss, stream) -> dict:
+    """Dense and 2:4-sparse tcgen05.mma rates with operands on chip (one CTA per
+    SM), in dense-equivalent TFLOP/s, for the instruction shapes the GEMMs use."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = {}
+    for dname, dt, eb in (("bf16", ss.BF16, 2), ("e4m3", ss.E4M3, 1)):
+        for n in (192, 256):
+            for sparse in (False, True):
+                iters = 16384
+                ss.mma_rate(dt, sparse, n, iters)
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(3):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    ss.mma_rate(dt, sparse, n, iters)
+                    b.record(stream)
+                    b.synchronize()
+                    ts.append(a.elapsed_time(b))
+                flops = sms * iters * 2.0 * 128 * n * (128 // eb)
+                out[f"{dname}_{'sparse' if sparse else 'dense'}_n{n}"] = round(flops / (min(ts) * 1e-3) / 1e12, 1)
+    assert ss.check_device_error() == 0, "device error flag set by the MMA microbenchmark"
+    return out
+
+
 def make_sp24(wl, dev, ss):
     d = wl.make()
     Wd = I.torch_view(d["W"], wl.dt).to(dev)
@@ -243,8 +269,10 @@ def run_gpu(args) -> None:
     e2e_value = ws * eff_flops / (statistics.mean(e2e_times) * 1e-3) / 1e12
 
     rows = {}
+    mma = None
     if not args.no_rows and rank == 0:
         rows = bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd)
+        mma = mma_microbench(ss, stream)
 
     if rank == 0:
         clocks = clk.summary()
@@ -267,10 +295,18 @@ def run_gpu(args) -> None:
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": int(Xd.numel() * Xd.element_size()),
                     "d2h_bytes_per_step": int(Y.numel() * Y.element_size())},
+            "mma_microbench_dense_equivalent_tflops": mma,
             "gpu_launches": args.steps,
             "clocks": clocks,
             "rows": rows,
         }
+        key = f"{wl.dt}_sparse_n192"
+        if mma and key in mma:
+            # the same ceiling as measured on chip at the headline's instruction shape
+            # (effective = dense-equivalent / 2)
+            mb = mma[key] / 2.0
+            line["roofline"]["peak_sparse_mma_microbench"] = round(mb, 1)
+            line["roofline"]["frac_of_microbench"] = round(achieved / mb, 4)
         if args.cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, d, args.cpu_seconds)
         print(json.dumps(line), flush=True)

@@ -74,6 +74,21 @@ int ssdnn_check_device_error(void* stream);
  * recovery path (kernels give up on a stalled pipeline instead of hanging). */
 int ssdnn_selftest_wait_timeout(uint32_t limit_us, void* stream);
 
+/* Tensor-core rate microbenchmark (measurement only; no output buffer).
+ * Launches one CTA per SM on `stream`; each issues `iters` (1 .. 262144) steps
+ * of tcgen05.mma with operands resident in shared memory and the fp32
+ * accumulator in TMEM: M = 128 rows, N = `n` columns (128, 192 or 256), and
+ * 128 bytes of K per step (64 elements for f16/bf16, 128 for e4m3), in the dense
+ * (`sparse` = 0) or the 2:4-sparse (`sparse` = 1) form, where K counts the dense
+ * width the sparse instruction covers. A step is 2 * 128 * n * (128 / elem
+ * bytes) dense-equivalent flops per SM; the caller times the launch. The pages
+ * state that the sparse tensor core doubles the dense math rate ("Accelerating
+ * Sparse Deep Neural Networks", Abstract; "NVIDIA A100 benchmarks" page, 2:4
+ * paragraph); this call measures both rates on the device at hand.
+ * Returns SSDNN_ERR_INVALID_ARG / SSDNN_ERR_UNSUPPORTED for a bad dtype, flag,
+ * step count or n, else the launch status. */
+int ssdnn_mma_rate(int dt, int sparse, int n, int iters, void* stream);
+
 /* ------------------------------------------------------------------ 2:4 ----
  * Compressed 2:4 layouts (Kp = round_up(K, 32)):
  *   values   M x Kp/2 elements, row-major: the kept values of each group in

@@ -44,4 +44,7 @@ cudaError_t launch_tw_prune(int dt, int tvw, const void* W, int64_t M, int64_t K
                             const int32_t* schedule, void* packed, uint8_t* meta, uint8_t* meta_hw,
                             float* scores, cudaStream_t s, uint32_t* err);
 
+// Tensor-core issue-rate microbenchmark (operands resident on chip), one CTA per SM.
+cudaError_t launch_mma_rate(int dt, int sparse, int n, int iters, cudaStream_t s, uint32_t* err);
+
 }  // namespace ssdnn

@@ -98,3 +98,8 @@ def test_argument_errors_before_any_device_work(ssdnn):
     # the wait-timeout self-test takes a limit of 1 us .. 1 s
     assert lib.ssdnn_selftest_wait_timeout(0, None) == 1
     assert lib.ssdnn_selftest_wait_timeout(1000001, None) == 1
+    # the tensor-core rate microbenchmark validates its arguments on the host
+    assert lib.ssdnn_mma_rate(7, 0, 128, 16, None) == 1
+    assert lib.ssdnn_mma_rate(1, 2, 128, 16, None) == 1
+    assert lib.ssdnn_mma_rate(1, 0, 128, 0, None) == 1
+    assert lib.ssdnn_mma_rate(1, 0, 96, 16, None) == 2

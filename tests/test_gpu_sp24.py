@@ -166,3 +166,15 @@ def test_bounded_wait_reports_timeout_without_fault():
     Y = ss.sp24_gemm(f, dev_tensor(X, "bf16"))
     assert np.array_equal(bits_of(Y), oracle.sp24.prune(W, "bf16"))
     assert ss.check_device_error() == 0
+
+
+@pytest.mark.parametrize("dt", ["bf16", "e4m3"])
+@pytest.mark.parametrize("sparse", [False, True])
+def test_mma_rate_microbenchmark_runs_clean(dt, sparse):
+    """The on-chip tensor-core rate kernel completes on every SM without a device
+    error, for each instruction shape the bench measures."""
+    ss = lib()
+    for n in (128, 192, 256):
+        ss.mma_rate(ss.BF16 if dt == "bf16" else ss.E4M3, sparse, n, 64)
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
