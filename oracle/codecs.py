@@ -84,20 +84,14 @@ def encode(x: np.ndarray, dt: str) -> np.ndarray:
         bits = (f >> np.uint32(16)).astype(np.uint16)
         return np.where(np.isnan(r), np.uint16(0x7FC0), bits).astype(np.uint16)
     if dt == "e4m3":
-        table = decode(np.arange(256, dtype=np.uint8), "e4m3")
-        finite_codes = np.array([c for c in range(256) if np.isfinite(table[c])], dtype=np.uint8)
-        vals = table[finite_codes]
-        out = np.zeros(r.shape, dtype=np.uint8)
-        flat_r = r.reshape(-1)
-        flat_o = out.reshape(-1)
-        for i, v in enumerate(flat_r):
-            if np.isnan(v):
-                flat_o[i] = 0x7F
-                continue
-            hits = finite_codes[vals == v]
-            if v == 0.0:   # keep the sign of zero
-                flat_o[i] = 0x80 if np.signbit(v) else 0x00
-            else:
-                flat_o[i] = hits[0]
-        return out
+        # r holds representable values only: look each magnitude up among the 127
+        # finite non-negative codes (ascending in value), then set the sign bit
+        pos = np.arange(127, dtype=np.uint8)                  # 0x00 .. 0x7E
+        vals = decode(pos, "e4m3")
+        mag = np.abs(r)
+        idx = np.clip(np.searchsorted(vals, np.where(np.isnan(mag), 0.0, mag)), 0, 126)
+        code = pos[idx]
+        assert np.all((vals[idx] == mag) | np.isnan(mag)), "value not representable in e4m3"
+        code = np.where(np.signbit(r), code | np.uint8(0x80), code).astype(np.uint8)
+        return np.where(np.isnan(r), np.uint8(0x7F), code).astype(np.uint8)
     raise ValueError(dt)

@@ -77,3 +77,15 @@ def test_decode_encode_roundtrip_exhaustive():
     v = codecs.decode(bits, "e4m3")
     fin = np.isfinite(v)
     assert (codecs.encode(v[fin], "e4m3") == bits[fin]).all()
+
+
+def test_e4m3_encode_matches_torch_cast_inside_the_finite_range():
+    """torch's fp32 -> float8_e4m3fn cast is an independent RNE implementation;
+    compared on fp32 values within +-448 (where saturation plays no part),
+    including the subnormal range and exact ties."""
+    rng = np.random.default_rng(1)
+    x = rng.uniform(-448, 448, 20000) * 2.0 ** rng.integers(-14, 1, 20000)
+    ties = np.array([1.0625, 1.1875, 2.0 ** -9 * 1.5, 2.0 ** -9 * 0.5, -2.0 ** -9 * 2.5, 240.0 + 8.0])
+    x = np.concatenate([x, ties]).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (codecs.encode(x, "e4m3") == ref).all()
