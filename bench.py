@@ -271,7 +271,7 @@ def run_gpu(args) -> None:
     rows = {}
     mma = None
     if not args.no_rows and rank == 0:
-        rows = bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd)
+        rows = bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form)
         mma = mma_microbench(ss, stream)
 
     if rank == 0:
@@ -315,7 +315,7 @@ def run_gpu(args) -> None:
         dist.destroy_process_group()
 
 
-def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd) -> dict:
+def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> dict:
     """Time the other hot-path rows on their own workloads."""
     rows = {}
     steps = max(5, args.steps // 2)
@@ -335,6 +335,21 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd) -> dict:
     rows["dense_gemm"] = {"workload": wl.name, "ms": round(t, 4), "TFLOP/s": round(dense_tf, 1),
                           "frac_of_dense_peak": round(dense_tf / (pk["bf16_tflops"] * (2 if wl.dt == "e4m3" else 1)),
                                                       3)}
+    # the fused layer epilogue on the same shape: per-row bias + GELU, e4m3 output
+    # (the next layer's input), against the plain GEMM with its bf16 output
+    if wl.dt == "e4m3":
+        Y8 = torch.empty((M, N), dtype=torch.float8_e4m3fn, device=dev)
+        bias = torch.linspace(-0.5, 0.5, M, dtype=torch.float32, device=dev)
+        t_ep = statistics.mean(timed_steps(
+            lambda: ss.sp24_gemm(form_main, Xd, alpha=d["alpha"], out=Y8, bias=bias, act="gelu", y_scale=8.0),
+            steps, 2, flush, stream))
+        t_plain = statistics.mean(timed_steps(lambda: ss.sp24_gemm(form_main, Xd, alpha=d["alpha"], out=Yd), steps,
+                                              2, flush, stream))
+        eff = M * N * K / (t_ep * 1e-3) / 1e12
+        rows["sp24_gemm_bias_gelu_e4m3_out"] = {"workload": wl.name, "ms": round(t_ep, 4),
+                                                "plain_bf16_out_ms": round(t_plain, 4),
+                                                "effective_TFLOP/s": round(eff, 1)}
+        del Y8, bias
     # a2 in bf16 on the same LLM FFN shape, when the headline is e4m3
     if wl.name == "llm_ffn_e4m3":
         wb = I.WORKLOADS["llm_ffn_bf16"]

@@ -173,6 +173,43 @@ int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* ke
              const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
              const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream);
 
+/* --------------------------------------------------- fused layer epilogue ----
+ * A pruned fully connected layer or 1x1 convolution runs as one of the GEMMs
+ * above ("Accelerating Sparse DNNs Based on Tiled GEMM", Abstract), and the step
+ * that follows it -- bias, activation, quantisation of the layer output -- is
+ * fused into the GEMM's epilogue ("kernel fusion", same page, TL;DR). Per output
+ * element, in fp32 and in this order:
+ *     z = alpha * acc + bias[row]       (one fma; without a bias: alpha * acc)
+ *     a = act(z)                        none | ReLU max(z, 0) | GELU 0.5 z (1 + erf(z / sqrt 2))
+ *     Y = round_out(y_scale * a)        ties to even; e4m3 saturates to +-448
+ * acc is the fp32 tensor-core accumulator; row indexes the output features (rows
+ * of W and of Y). For e4m3 output, y_scale is the reciprocal of the output
+ * tensor's quantisation scale. With K == 0 (or no kept column at all) acc = 0. */
+typedef enum { SSDNN_ACT_NONE = 0, SSDNN_ACT_RELU = 1, SSDNN_ACT_GELU = 2 } ssdnn_act;
+
+typedef struct ssdnn_epilogue {
+  const float* bias; /* device, M floats (one per output row), 4-byte aligned; NULL = no bias */
+  int act;           /* ssdnn_act */
+  float y_scale;     /* finite multiplier after the activation (1.0f = none) */
+} ssdnn_epilogue;
+
+/* sp24_gemm / dense_gemm / tvw_gemm with the fused epilogue `ep` (NULL = the
+ * plain conversion). out_dt may also be SSDNN_E4M3 here (ldy * out bytes a
+ * multiple of 16). Returns SSDNN_ERR_INVALID_ARG for an unknown activation or a
+ * non-finite y_scale, SSDNN_ERR_UNSUPPORTED for a misaligned bias; otherwise as
+ * the plain call. tvw_gemm_ep adds the output type and alpha that tvw_gemm
+ * fixes to dt and 1. */
+int sp24_gemm_ep(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+                 const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                 const ssdnn_epilogue* ep, void* stream);
+int dense_gemm_ep(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
+                  const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+                  void* stream);
+int tvw_gemm_ep(int dt, int out_dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* keep_counts_host,
+                const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+                const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                const ssdnn_epilogue* ep, void* stream);
+
 /* ------------------------------------------------- allocation-free variant ----
  * tw_prune_compress_noalloc: tw_prune_compress for callers that cannot allocate
  * device memory. (The pages have no counterpart: this is a deployment aid.)

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -51,23 +52,51 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? SSDNN_OK : SSDNN_ERR_CUDA; }
 
+int out_bytes(int out_dt) { return out_dt == SSDNN_E4M3 ? 1 : 2; }
+
 // Zero the M x N output (K == 0 or no kept columns anywhere).
-int zero_output(void* Y, int64_t ldy, int64_t M, int64_t N, cudaStream_t s) {
+int zero_output(void* Y, int64_t ldy, int64_t M, int64_t N, int ob, cudaStream_t s) {
   if (M == 0 || N == 0) return SSDNN_OK;
-  return from_cuda(cudaMemset2DAsync(Y, static_cast<size_t>(ldy * 2), 0, static_cast<size_t>(N * 2),
+  return from_cuda(cudaMemset2DAsync(Y, static_cast<size_t>(ldy * ob), 0, static_cast<size_t>(N * ob),
                                      static_cast<size_t>(M), s));
 }
 
-int check_gemm_io(int out_dt, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, int eb, void* Y,
-                  int64_t ldy) {
-  if (out_dt != SSDNN_F16 && out_dt != SSDNN_BF16) return SSDNN_ERR_UNSUPPORTED;
+// Output checks shared by the GEMMs; e4m3 output only through the epilogue entry points.
+int check_gemm_io(int out_dt, bool f8_out_ok, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, int eb,
+                  void* Y, int64_t ldy) {
+  if (out_dt != SSDNN_F16 && out_dt != SSDNN_BF16 && !(f8_out_ok && out_dt == SSDNN_E4M3))
+    return SSDNN_ERR_UNSUPPORTED;
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SSDNN_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SSDNN_OK;
   if (!Y || (K > 0 && !X)) return SSDNN_ERR_INVALID_ARG;
   if (ldy < N || (K > 0 && ldx < N)) return SSDNN_ERR_INVALID_ARG;
-  if (!aligned16(Y) || (ldy * 2) % 16) return SSDNN_ERR_UNSUPPORTED;
+  if (!aligned16(Y) || (ldy * out_bytes(out_dt)) % 16) return SSDNN_ERR_UNSUPPORTED;
   if (K > 0 && (!aligned16(X) || (ldx * eb) % 16)) return SSDNN_ERR_UNSUPPORTED;
   return SSDNN_OK;
+}
+
+int check_epilogue(const ssdnn_epilogue* ep) {
+  if (!ep) return SSDNN_OK;
+  if (ep->act < SSDNN_ACT_NONE || ep->act > SSDNN_ACT_GELU || !std::isfinite(ep->y_scale))
+    return SSDNN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ep->bias) & 3u) return SSDNN_ERR_UNSUPPORTED;
+  return SSDNN_OK;
+}
+
+void set_epilogue(GemmArgs& a, const ssdnn_epilogue* ep) {
+  if (!ep) return;
+  a.bias = ep->bias;
+  a.act = ep->act;
+  a.y_scale = ep->y_scale;
+}
+
+// A product with no terms: Y = round(y_scale * act(bias[row])), zeros without a bias
+// (every activation maps 0 to 0).
+int empty_product(void* Y, int64_t ldy, int64_t M, int64_t N, int out_dt, const ssdnn_epilogue* ep,
+                  cudaStream_t s) {
+  if (ep && ep->bias)
+    return from_cuda(launch_fill_epilogue(Y, ldy, M, N, out_dt, ep->bias, ep->act, ep->y_scale, s));
+  return zero_output(Y, ldy, M, N, out_bytes(out_dt), s);
 }
 
 struct Tables {
@@ -115,6 +144,104 @@ int build_tables(int tvw, int64_t M, int64_t K, const int32_t* keep, Tables* out
 }
 
 }  // namespace
+int sp24_gemm_impl(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+                   const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                   const ssdnn_epilogue* ep, bool f8_out_ok, void* stream) {
+  if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
+  const int eb = elem_bytes(in_dt);
+  int st = check_gemm_io(out_dt, f8_out_ok, M, N, K, X, ldx, eb, Y, ldy);
+  if (st == SSDNN_OK) st = check_epilogue(ep);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (K % 4) return SSDNN_ERR_UNSUPPORTED;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return empty_product(Y, ldy, M, N, out_dt, ep, s);
+  if (!values || !meta_hw) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(values) || !aligned16(meta_hw)) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = in_dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = values;
+  a.lda = round_up(K, 32) / 2;
+  a.meta_hw = meta_hw;
+  a.X = X;
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  set_epilogue(a, ep);
+  return from_cuda(launch_gemm(1, a, s, error_word()));
+}
+
+int dense_gemm_impl(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
+                    const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+                    bool f8_out_ok, void* stream) {
+  if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
+  const int eb = elem_bytes(in_dt);
+  int st = check_gemm_io(out_dt, f8_out_ok, M, N, K, X, ldx, eb, Y, ldy);
+  if (st == SSDNN_OK) st = check_epilogue(ep);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return empty_product(Y, ldy, M, N, out_dt, ep, s);
+  if (!W || ldw < K) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(W) || (ldw * eb) % 16) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = in_dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = W;
+  a.lda = ldw;
+  a.X = X;
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  set_epilogue(a, ep);
+  return from_cuda(launch_gemm(0, a, s, error_word()));
+}
+
+int tvw_gemm_impl(int dt, int out_dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* keep_counts_host,
+                  const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+                  const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                  const ssdnn_epilogue* ep, bool f8_out_ok, void* stream) {
+  if (dt != SSDNN_F16 && dt != SSDNN_BF16) return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  int st = check_gemm_io(out_dt, f8_out_ok, M, N, K, X, ldx, 2, Y, ldy);
+  if (st == SSDNN_OK) st = check_epilogue(ep);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (!keep_counts_host) return SSDNN_ERR_INVALID_ARG;
+  Tables tb;
+  st = build_tables(tvw, M, K, keep_counts_host, &tb);
+  if (st != SSDNN_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0 || tb.t.P_total == 0) return empty_product(Y, ldy, M, N, out_dt, ep, s);
+  if (!offsets || !indices || !schedule || !packed || (tvw && !meta_hw)) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(packed) || (tvw && !aligned16(meta_hw))) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = packed;
+  a.meta_hw = meta_hw;
+  a.X = X;
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  a.nt = tb.t.nt;
+  a.packed_rows = 2 * tb.t.P_total;
+  a.offsets = offsets;
+  a.indices = indices;
+  a.schedule = schedule;
+  set_epilogue(a, ep);
+  return from_cuda(launch_gemm(tvw ? 3 : 2, a, s, error_word()));
+}
+
 }  // namespace ssdnn
 
 using namespace ssdnn;
@@ -195,56 +322,24 @@ int sp24_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw
 int sp24_gemm(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
               const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
               void* stream) {
-  if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
-  const int eb = elem_bytes(in_dt);
-  int st = check_gemm_io(out_dt, M, N, K, X, ldx, eb, Y, ldy);
-  if (st != SSDNN_OK || M == 0 || N == 0) return st;
-  if (K % 4) return SSDNN_ERR_UNSUPPORTED;
-  auto s = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(Y, ldy, M, N, s);
-  if (!values || !meta_hw) return SSDNN_ERR_INVALID_ARG;
-  if (!aligned16(values) || !aligned16(meta_hw)) return SSDNN_ERR_UNSUPPORTED;
-  GemmArgs a{};
-  a.dt = in_dt;
-  a.out_dt = out_dt;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.A = values;
-  a.lda = round_up(K, 32) / 2;
-  a.meta_hw = meta_hw;
-  a.X = X;
-  a.ldx = ldx;
-  a.Y = Y;
-  a.ldy = ldy;
-  a.alpha = alpha;
-  return from_cuda(launch_gemm(1, a, s, error_word()));
+  return sp24_gemm_impl(in_dt, out_dt, M, N, K, values, meta_hw, X, ldx, Y, ldy, alpha, nullptr, false, stream);
+}
+
+int sp24_gemm_ep(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+                 const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                 const ssdnn_epilogue* ep, void* stream) {
+  return sp24_gemm_impl(in_dt, out_dt, M, N, K, values, meta_hw, X, ldx, Y, ldy, alpha, ep, true, stream);
 }
 
 int dense_gemm(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
                const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, void* stream) {
-  if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
-  const int eb = elem_bytes(in_dt);
-  int st = check_gemm_io(out_dt, M, N, K, X, ldx, eb, Y, ldy);
-  if (st != SSDNN_OK || M == 0 || N == 0) return st;
-  auto s = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(Y, ldy, M, N, s);
-  if (!W || ldw < K) return SSDNN_ERR_INVALID_ARG;
-  if (!aligned16(W) || (ldw * eb) % 16) return SSDNN_ERR_UNSUPPORTED;
-  GemmArgs a{};
-  a.dt = in_dt;
-  a.out_dt = out_dt;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.A = W;
-  a.lda = ldw;
-  a.X = X;
-  a.ldx = ldx;
-  a.Y = Y;
-  a.ldy = ldy;
-  a.alpha = alpha;
-  return from_cuda(launch_gemm(0, a, s, error_word()));
+  return dense_gemm_impl(in_dt, out_dt, M, N, K, W, ldw, X, ldx, Y, ldy, alpha, nullptr, false, stream);
+}
+
+int dense_gemm_ep(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
+                  const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+                  void* stream) {
+  return dense_gemm_impl(in_dt, out_dt, M, N, K, W, ldw, X, ldx, Y, ldy, alpha, ep, true, stream);
 }
 
 int tw_sizes(int dt, int tvw, int64_t M, int64_t K, const int32_t* keep_counts_host, size_t* packed_bytes,
@@ -297,36 +392,16 @@ int tw_prune_compress(int dt, int tvw, const void* W, int64_t M, int64_t K, int6
 int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* keep_counts_host,
              const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
              const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream) {
-  if (dt != SSDNN_F16 && dt != SSDNN_BF16) return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
-  int st = check_gemm_io(dt, M, N, K, X, ldx, 2, Y, ldy);
-  if (st != SSDNN_OK || M == 0 || N == 0) return st;
-  if (!keep_counts_host) return SSDNN_ERR_INVALID_ARG;
-  Tables tb;
-  st = build_tables(tvw, M, K, keep_counts_host, &tb);
-  if (st != SSDNN_OK) return st;
-  auto s = static_cast<cudaStream_t>(stream);
-  if (K == 0 || tb.t.P_total == 0) return zero_output(Y, ldy, M, N, s);
-  if (!offsets || !indices || !schedule || !packed || (tvw && !meta_hw)) return SSDNN_ERR_INVALID_ARG;
-  if (!aligned16(packed) || (tvw && !aligned16(meta_hw))) return SSDNN_ERR_UNSUPPORTED;
-  GemmArgs a{};
-  a.dt = dt;
-  a.out_dt = dt;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.A = packed;
-  a.meta_hw = meta_hw;
-  a.X = X;
-  a.ldx = ldx;
-  a.Y = Y;
-  a.ldy = ldy;
-  a.alpha = 1.0f;
-  a.nt = tb.t.nt;
-  a.packed_rows = 2 * tb.t.P_total;
-  a.offsets = offsets;
-  a.indices = indices;
-  a.schedule = schedule;
-  return from_cuda(launch_gemm(tvw ? 3 : 2, a, s, error_word()));
+  return tvw_gemm_impl(dt, dt, tvw, M, N, K, keep_counts_host, offsets, indices, schedule, packed, meta_hw, X, ldx,
+                       Y, ldy, 1.0f, nullptr, false, stream);
+}
+
+int tvw_gemm_ep(int dt, int out_dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* keep_counts_host,
+                const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+                const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                const ssdnn_epilogue* ep, void* stream) {
+  return tvw_gemm_impl(dt, out_dt, tvw, M, N, K, keep_counts_host, offsets, indices, schedule, packed, meta_hw, X,
+                       ldx, Y, ldy, alpha, ep, true, stream);
 }
 
 }  // extern "C"

@@ -36,6 +36,7 @@
 //        four TMEM columns; instruction j reads its metadata at column 2 j.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 #include <cstdlib>
@@ -54,7 +55,10 @@ struct Params {
   int32_t GR;               // rasterisation: M groups per band; work sweeps a band's N blocks
   int32_t num_units;        // work items: (M group, N block) pairs, or (schedule entry, N block)
   int32_t nk;               // k stages per unit (dense / sp24)
-  int32_t out_dt;           // 0 f16, 1 bf16
+  int32_t out_dt;           // 0 f16, 1 bf16, 2 e4m3
+  int32_t act;              // fused epilogue: 0 none, 1 ReLU, 2 GELU
+  const float* bias;        // fused epilogue: one fp32 bias per output row, or null
+  float y_scale;            // fused epilogue: multiplier after the activation
   int32_t nstages;          // stages of the shared-memory ring in use (<= the compiled count)
   float alpha;
   const uint8_t* meta_hw;
@@ -169,6 +173,68 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
     ui.L = L;
   }
   return ui;
+}
+
+// The fused layer epilogue on one fp32 accumulator value, in this order: alpha
+// times the accumulator plus the row's bias (one fma), the activation, the
+// output scale. GELU is the exact form 0.5 x (1 + erf(x / sqrt 2)).
+__device__ __forceinline__ float epilogue_value(float acc, float alpha, float b, bool has_bias, int act,
+                                               float y_scale) {
+  float x = has_bias ? fmaf(acc, alpha, b) : acc * alpha;
+  if (act == 1) {
+    x = x > 0.f ? x : 0.f;
+  } else if (act == 2) {
+    x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+  }
+  return x * y_scale;
+}
+
+// Rounds 32 consecutive outputs of one row (ties to even; e4m3 saturating) and
+// stores them at dst (columns n0 .. n0 + 31, those below N).
+__device__ __forceinline__ void store_row32(uint8_t* dst_row, int32_t n0, int32_t N, int out_dt, const float (&x)[32],
+                                            uint64_t pol) {
+  if (out_dt == 2) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i], x[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i + 2], x[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
+      w[i] = (lo & 0xFFFFu) | (hi << 16);
+    }
+    uint8_t* dst = dst_row + n0;
+    if (n0 + 32 <= N) {
+      ptx::st_global_v4_hint(dst, w[0], w[1], w[2], w[3], pol);
+      ptx::st_global_v4_hint(dst + 16, w[4], w[5], w[6], w[7], pol);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < N) dst[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+    }
+    return;
+  }
+  uint32_t packed[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (out_dt == 1) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+      packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+      packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+  uint16_t* dst = reinterpret_cast<uint16_t*>(dst_row) + n0;
+  if (n0 + 32 <= N) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      ptx::st_global_v4_hint(reinterpret_cast<uint4*>(dst) + v, packed[4 * v], packed[4 * v + 1],
+                             packed[4 * v + 2], packed[4 * v + 3], pol);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (n0 + i < N) dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
+  }
 }
 
 template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW>
@@ -461,7 +527,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
       ptx::tc_fence_after();
       const int32_t row = ui.m0 + static_cast<int32_t>(128 * mt + 32 * q + lane);
       const bool row_ok = row < p.M && !ui.phantom;
-      uint8_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy * 2;
+      uint8_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy * (p.out_dt == 2 ? 1 : 2);
+      const bool has_bias = p.bias != nullptr;
+      const float bias = (has_bias && row_ok) ? __ldg(p.bias + row) : 0.f;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -479,30 +547,11 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
         }
         const int32_t n0 = ui.n0 + 32 * c;
         if (!row_ok || n0 >= p.N) continue;
-        uint32_t packed[16];
+        float x[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = __uint_as_float(r[2 * i]) * p.alpha;
-          const float x1 = __uint_as_float(r[2 * i + 1]) * p.alpha;
-          if (p.out_dt == 1) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-            packed[i] = *reinterpret_cast<const uint32_t*>(&h);
-          } else {
-            const __half2 h = __floats2half2_rn(x0, x1);
-            packed[i] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-        }
-        uint16_t* dst = reinterpret_cast<uint16_t*>(yrow) + n0;
-        if (n0 + 32 <= p.N) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            ptx::st_global_v4_hint(reinterpret_cast<uint4*>(dst) + v, packed[4 * v], packed[4 * v + 1],
-                                   packed[4 * v + 2], packed[4 * v + 3], pol_y);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (n0 + i < p.N) dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
-        }
+        for (int i = 0; i < 32; ++i)
+          x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, p.act, p.y_scale);
+        store_row32(yrow, n0, p.N, p.out_dt, x, pol_y);
       }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
     }
@@ -595,7 +644,10 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   }
   p.nk = static_cast<int32_t>(ceil_div(a.K, C::BK));
   p.num_units = GATHER ? static_cast<int32_t>(a.nt) * p.NB : p.MG * p.NB;
-  p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : 0;
+  p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : (a.out_dt == SSDNN_E4M3 ? 2 : 0);
+  p.act = a.act;
+  p.bias = a.bias;
+  p.y_scale = a.y_scale;
   p.nstages = C::STAGES;
   if (const char* e = getenv("SSDNN_STAGES")) {  // tuning: a shorter ring than shared memory allows
     const int v = atoi(e);
@@ -740,7 +792,37 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
   return cudaErrorInvalidValue;
 }
 
+__global__ void k_fill_epilogue(uint8_t* __restrict__ Y, int64_t ldy, int64_t M, int64_t N, int out_dt,
+                                const float* __restrict__ bias, int act, float y_scale) {
+  const bool hb = bias != nullptr;
+  for (int64_t row = blockIdx.y; row < M; row += gridDim.y) {
+    const float v = epilogue_value(0.f, 1.f, hb ? __ldg(bias + row) : 0.f, hb, act, y_scale);
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < N;
+         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      if (out_dt == 2) {
+        Y[row * ldy + j] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+      } else if (out_dt == 1) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        reinterpret_cast<__nv_bfloat16*>(Y)[row * ldy + j] = h;
+      } else {
+        const __half h = __float2half_rn(v);
+        reinterpret_cast<__half*>(Y)[row * ldy + j] = h;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fill_epilogue(void* Y, int64_t ldy, int64_t M, int64_t N, int out_dt, const float* bias, int act,
+                                 float y_scale, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const int code = out_dt == SSDNN_BF16 ? 1 : (out_dt == SSDNN_E4M3 ? 2 : 0);
+  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(ceil_div(N, 256), 64)),
+                  static_cast<unsigned>(std::min<int64_t>(M, 65535)));
+  k_fill_epilogue<<<grid, 256, 0, s>>>(static_cast<uint8_t*>(Y), ldy, M, N, code, bias, act, y_scale);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   switch (a.dt) {

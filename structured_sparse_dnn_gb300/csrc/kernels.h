@@ -27,10 +27,19 @@ struct GemmArgs {
   const int32_t* offsets;
   const int32_t* indices;
   const int32_t* schedule;
+  // fused layer epilogue (out = round(y_scale * act(alpha * acc + bias[row])))
+  const float* bias = nullptr;
+  int act = 0;          // 0 none, 1 ReLU, 2 GELU
+  float y_scale = 1.0f;
 };
 
 // mode: 0 dense, 1 sp24, 2 TW (dense packed + gather), 3 TVW (2:4 packed + gather)
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err);
+
+// Y = round(y_scale * act(bias[row])) for every element (the fused epilogue of a
+// product with no terms, K == 0); out_dt 0 f16, 1 bf16, 2 e4m3.
+cudaError_t launch_fill_epilogue(void* Y, int64_t ldy, int64_t M, int64_t N, int out_dt, const float* bias, int act,
+                                 float y_scale, cudaStream_t s);
 
 // Tile-wise prune: scores -> per-tile top-L selection -> pack (TVW: + 2:4).
 struct TwTables {

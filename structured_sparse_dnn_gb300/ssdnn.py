@@ -26,6 +26,16 @@ _DT = {torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3}
 _TORCH = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.float8_e4m3fn}
 
 _i64, _ptr, _sz, _i32p = C.c_int64, C.c_void_p, C.c_size_t, C.POINTER(C.c_int32)
+
+ACT = {"none": 0, "relu": 1, "gelu": 2}
+
+
+class Epilogue(C.Structure):
+    """ssdnn_epilogue: per-row fp32 bias (device pointer or None), activation, output scale."""
+    _fields_ = [("bias", C.c_void_p), ("act", C.c_int), ("y_scale", C.c_float)]
+
+
+_epp = C.POINTER(Epilogue)
 _SIGS = {
     "ssdnn_status_str": ([C.c_int], C.c_char_p),
     "ssdnn_version": ([], C.c_int),
@@ -38,6 +48,12 @@ _SIGS = {
                   C.c_int),
     "dense_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, C.c_float, _ptr],
                    C.c_int),
+    "sp24_gemm_ep": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _i64, _ptr, _i64, C.c_float, _epp,
+                      _ptr], C.c_int),
+    "dense_gemm_ep": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, C.c_float, _epp,
+                       _ptr], C.c_int),
+    "tvw_gemm_ep": ([C.c_int, C.c_int, C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64,
+                     _ptr, _i64, C.c_float, _epp, _ptr], C.c_int),
     "tw_sizes": ([C.c_int, C.c_int, _i64, _i64, _i32p, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz),
                   C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "tw_prune_compress": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
@@ -140,30 +156,51 @@ def sp24_prune_compress(W: torch.Tensor, canonical_meta: bool = True) -> Sp24:
     return Sp24(dt, M, K, values, meta, meta_hw[:hb])
 
 
+def _epilogue(bias: torch.Tensor | None, act: str, y_scale: float, M: int):
+    """The ssdnn_epilogue for these arguments, or None for the plain conversion."""
+    if bias is None and act == "none" and y_scale == 1.0:
+        return None
+    if bias is not None:
+        assert bias.dtype == torch.float32 and bias.is_cuda and bias.numel() == M and bias.is_contiguous()
+    return Epilogue(None if bias is None else bias.data_ptr(), ACT[act], float(y_scale))
+
+
 def sp24_gemm(form: Sp24, X: torch.Tensor, out_dtype: torch.dtype | None = None, alpha: float = 1.0,
-              out: torch.Tensor | None = None):
-    """Y = alpha * decompress(form) . X  (M x N)."""
+              out: torch.Tensor | None = None, bias: torch.Tensor | None = None, act: str = "none",
+              y_scale: float = 1.0):
+    """Y = round(y_scale * act(alpha * decompress(form) . X + bias[:, None]))  (M x N)."""
     dt = _DT[X.dtype]
     assert dt == form.dt and X.shape[0] == form.K
     N = X.shape[1]
     out_dtype = out_dtype or (torch.bfloat16 if dt == E4M3 else X.dtype)
     if out is None:
         out = torch.empty((form.M, N), dtype=out_dtype, device=X.device)
-    _check(lib.sp24_gemm(dt, _DT[out.dtype], form.M, N, form.K, _p(form.values), _p(form.meta_hw), _p(X),
-                         X.stride(0), _p(out), out.stride(0), alpha, _stream(X.device)), "sp24_gemm")
+    ep = _epilogue(bias, act, y_scale, form.M)
+    args = (dt, _DT[out.dtype], form.M, N, form.K, _p(form.values), _p(form.meta_hw), _p(X), X.stride(0), _p(out),
+            out.stride(0), alpha)
+    if ep is None and out.dtype != torch.float8_e4m3fn:
+        _check(lib.sp24_gemm(*args, _stream(X.device)), "sp24_gemm")
+    else:
+        _check(lib.sp24_gemm_ep(*args, None if ep is None else C.byref(ep), _stream(X.device)), "sp24_gemm_ep")
     return out
 
 
 def dense_gemm(W: torch.Tensor, X: torch.Tensor, out_dtype: torch.dtype | None = None, alpha: float = 1.0,
-               out: torch.Tensor | None = None):
+               out: torch.Tensor | None = None, bias: torch.Tensor | None = None, act: str = "none",
+               y_scale: float = 1.0):
+    """Y = round(y_scale * act(alpha * W . X + bias[:, None])) on the dense tensor cores."""
     dt = _DT[W.dtype]
     M, K = W.shape
     N = X.shape[1]
     out_dtype = out_dtype or (torch.bfloat16 if dt == E4M3 else W.dtype)
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=X.device)
-    _check(lib.dense_gemm(dt, _DT[out.dtype], M, N, K, _p(W), W.stride(0), _p(X), X.stride(0), _p(out),
-                          out.stride(0), alpha, _stream(X.device)), "dense_gemm")
+    ep = _epilogue(bias, act, y_scale, M)
+    args = (dt, _DT[out.dtype], M, N, K, _p(W), W.stride(0), _p(X), X.stride(0), _p(out), out.stride(0), alpha)
+    if ep is None and out.dtype != torch.float8_e4m3fn:
+        _check(lib.dense_gemm(*args, _stream(X.device)), "dense_gemm")
+    else:
+        _check(lib.dense_gemm_ep(*args, None if ep is None else C.byref(ep), _stream(X.device)), "dense_gemm_ep")
     return out
 
 
@@ -244,11 +281,19 @@ def tw_prune_compress_noalloc(W: torch.Tensor, keep, tvw: bool) -> TileWise:
                     None if meta_hw is None else meta_hw[:sz["meta_hw_bytes"]])
 
 
-def tvw_gemm(form: TileWise, X: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+def tvw_gemm(form: TileWise, X: torch.Tensor, out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+             alpha: float = 1.0, bias: torch.Tensor | None = None, act: str = "none", y_scale: float = 1.0):
+    """Y = W_tw . X[idx] per tile (TW), or its 2:4 form (TVW); with the fused
+    epilogue when bias / act / y_scale / alpha / an e4m3 output are given."""
     N = X.shape[1]
     if out is None:
-        out = torch.empty((form.M, N), dtype=X.dtype, device=X.device)
-    _check(lib.tvw_gemm(form.dt, int(form.tvw), form.M, N, form.K, _kp(form.keep), _p(form.offsets),
-                        _p(form.indices), _p(form.schedule), _p(form.packed), _p(form.meta_hw), _p(X),
-                        X.stride(0), _p(out), out.stride(0), _stream(X.device)), "tvw_gemm")
+        out = torch.empty((form.M, N), dtype=out_dtype or X.dtype, device=X.device)
+    ep = _epilogue(bias, act, y_scale, form.M)
+    tail = (_kp(form.keep), _p(form.offsets), _p(form.indices), _p(form.schedule), _p(form.packed),
+            _p(form.meta_hw), _p(X), X.stride(0), _p(out), out.stride(0))
+    if ep is None and out.dtype == X.dtype and alpha == 1.0:
+        _check(lib.tvw_gemm(form.dt, int(form.tvw), form.M, N, form.K, *tail, _stream(X.device)), "tvw_gemm")
+    else:
+        _check(lib.tvw_gemm_ep(form.dt, _DT[out.dtype], int(form.tvw), form.M, N, form.K, *tail, alpha,
+                               None if ep is None else C.byref(ep), _stream(X.device)), "tvw_gemm_ep")
     return out

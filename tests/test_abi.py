@@ -103,3 +103,13 @@ def test_argument_errors_before_any_device_work(ssdnn):
     assert lib.ssdnn_mma_rate(1, 2, 128, 16, None) == 1
     assert lib.ssdnn_mma_rate(1, 0, 128, 0, None) == 1
     assert lib.ssdnn_mma_rate(1, 0, 96, 16, None) == 2
+    # fused epilogue: unknown activation, non-finite scale, misaligned bias, e4m3 pitch
+    import ctypes as C
+    ep = ssdnn.Epilogue(None, 5, 1.0)
+    assert lib.dense_gemm_ep(0, 0, 4, 8, 8, 16, 8, 16, 8, 16, 8, 1.0, C.byref(ep), None) == 1
+    ep = ssdnn.Epilogue(None, 1, float("inf"))
+    assert lib.sp24_gemm_ep(0, 0, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, C.byref(ep), None) == 1
+    ep = ssdnn.Epilogue(2, 1, 1.0)
+    assert lib.sp24_gemm_ep(0, 0, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, C.byref(ep), None) == 2
+    assert lib.sp24_gemm_ep(0, 2, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, None, None) == 2      # e4m3 row pitch 8 B
+    assert lib.sp24_gemm(0, 2, 4, 16, 8, 16, 16, 16, 16, 16, 16, 1.0, None) == 2          # plain call: no e4m3 out
