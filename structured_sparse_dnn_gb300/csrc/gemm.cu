@@ -72,9 +72,15 @@ struct Params {
   uint32_t* err;
 };
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128, bool PAIR = false>
 struct Cfg {
-  static constexpr int CLUSTER = CS;                        // CTAs sharing one X panel by multicast
+  // PAIR: the two CTAs of a cluster form an SM pair running M = 256 MMAs (each CTA
+  // holds 128 rows of A, BN/2 columns of B and its 128 accumulator rows); else
+  // CS > 1 CTAs of a cluster share one X panel by multicast.
+  static constexpr bool PAIRED = PAIR;
+  static constexpr int CLUSTER = PAIR ? 2 : CS;             // CTAs per cluster
+  static constexpr bool MCAST = !PAIR && CS > 1;
+  static constexpr int BN_CTA = PAIR ? BN / 2 : BN;         // B columns held by this CTA
   static constexpr int SUB = MT;                            // 128-row sub-tiles per CTA tile
   static constexpr int BM = 128 * MT;
   // 4 control warps, 4 epilogue warps per sub-tile, and for TW/TVW 4 warps that
@@ -93,10 +99,15 @@ struct Cfg {
   static constexpr int BK = 128 / EB;                       // dense K per stage
   static constexpr int A_SUB_BYTES = SPARSE ? 128 * 64 : 128 * 128;
   static constexpr int A_BYTES = MT * A_SUB_BYTES;
-  static constexpr int B_BYTES = 128 * BN;                  // BK * BN * EB
+  static constexpr int B_BYTES = 128 * BN_CTA;              // BK * BN_CTA * EB
   static constexpr int META_BYTES = SPARSE ? 2048 * MT : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + META_BYTES;
-  static constexpr int STAGES_RAW = (220 * 1024) / STAGE_BYTES;
+  // Output staging (all but TW/TVW): each epilogue warp converts a 32 x 32 chunk
+  // into one of two 2 KB shared-memory buffers and a TMA store writes it out, so
+  // the accumulator is drained without waiting on global stores.
+  static constexpr bool STAGED = !GATHER;
+  static constexpr int STAGING_BYTES = STAGED ? 4 * MT * 4096 : 0;
+  static constexpr int STAGES_RAW = (220 * 1024 - STAGING_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int MMA_K = (SPARSE ? 64 : 32) / EB;      // dense K per instruction
   static constexpr int MMAS = BK / MMA_K;                    // instructions per stage
@@ -104,7 +115,7 @@ struct Cfg {
   // lets an e4m3 N tile be a multiple of 64 columns)
   static constexpr int B_ROW = BROW;
   static constexpr int B_BOX_COLS = BROW / EB;               // columns per B box
-  static constexpr int B_BOXES = BN / B_BOX_COLS;
+  static constexpr int B_BOXES = BN_CTA / B_BOX_COLS;
   static constexpr int B_BOX_BYTES = BK * BROW;
   static constexpr int B_SBO = 8 * BROW;                     // 8-row swizzle atom
   static constexpr uint32_t B_SWZ = BROW == 128 ? 2u : 4u;
@@ -116,16 +127,24 @@ struct Cfg {
   static constexpr int NACC = (2 * ACC_COLS + META_COLS <= 512) ? 2 : 1;
   static constexpr int META_COL0 = NACC * ACC_COLS;         // TMEM columns after the accumulators
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t IDESC = ptx::idesc(Elem<DT>::mma_fmt, Elem<DT>::mma_fmt, SPARSE, 128, BN,
-                                               false, true);
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-  static_assert(B_BOXES * B_BOX_COLS == BN, "BN must be a multiple of the B box width");
+  static constexpr uint32_t IDESC = ptx::idesc(Elem<DT>::mma_fmt, Elem<DT>::mma_fmt, SPARSE, PAIR ? 256 : 128,
+                                               BN, false, true);
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(STAGES >= 2, "the shared-memory ring needs two stages");
+  static_assert(B_BOXES * B_BOX_COLS == BN_CTA, "BN must be a multiple of the B box width");
+  static_assert(!PAIR || (MT == 1 && CS == 1 && !GATHER), "SM pairs: one 128-row sub-tile per CTA");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
   static_assert(MT == 1 || (CS == 1 && !GATHER), "256-row tiles: no cluster, no gather");
   static_assert(CS == 1 || !GATHER, "gathered B rows differ per tile: no multicast");
-  static constexpr int B_SLICE_ROWS = BK / CS;              // rows of each B box this CTA loads
+  static constexpr int B_SLICE_ROWS = BK / (MCAST ? CS : 1); // rows of each B box this CTA loads
   static_assert(B_SLICE_ROWS % 8 == 0, "B slices must keep whole 8-row swizzle atoms");
 };
+
+// N width of one output tile (both CTAs of a pair write all of it for their rows).
+template <typename C>
+__device__ __forceinline__ constexpr int BN_OF() {
+  return C::BN_CTA * (C::PAIRED ? 2 : 1);
+}
 
 struct UnitInfo {
   int32_t m0, n0, nk;
@@ -150,7 +169,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
     const int32_t mb = mg * C::CLUSTER + static_cast<int32_t>(crank);
     ui.phantom = mb >= p.MB;
     ui.m0 = mb * C::BM;
-    ui.n0 = nb * (C::B_BOXES * C::B_BOX_COLS);
+    ui.n0 = nb * BN_OF<C>();
     ui.nk = p.nk;
     ui.a_row0 = ui.m0;
     // one 2048-byte metadata block per (128-row block, stage)
@@ -165,7 +184,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
     ui.phantom = false;
     ui.subs = 1;
     ui.m0 = t * 128;
-    ui.n0 = nb * (C::B_BOXES * C::B_BOX_COLS);
+    ui.n0 = nb * BN_OF<C>();
     ui.nk = (L + C::BK - 1) / C::BK;
     ui.a_row0 = 2 * P;  // packed chunks: 128 rows each, tile t starts at row 2 P
     ui.meta_blk0 = Q;
@@ -189,12 +208,11 @@ __device__ __forceinline__ float epilogue_value(float acc, float alpha, float b,
   return x * y_scale;
 }
 
-// Rounds 32 consecutive outputs of one row (ties to even; e4m3 saturating) and
-// stores them at dst (columns n0 .. n0 + 31, those below N).
-__device__ __forceinline__ void store_row32(uint8_t* dst_row, int32_t n0, int32_t N, int out_dt, const float (&x)[32],
-                                            uint64_t pol) {
+// Rounds 32 consecutive outputs of one row to the output type (ties to even; e4m3
+// saturating) and packs them: 16 words of fp16/bf16 pairs, or 8 words of e4m3
+// quads (words 8..15 unused).
+__device__ __forceinline__ void pack_row32(int out_dt, const float (&x)[32], uint32_t (&w)[16]) {
   if (out_dt == 2) {
-    uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i], x[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
@@ -202,6 +220,26 @@ __device__ __forceinline__ void store_row32(uint8_t* dst_row, int32_t n0, int32_
           __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i + 2], x[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
       w[i] = (lo & 0xFFFFu) | (hi << 16);
     }
+#pragma unroll
+    for (int i = 8; i < 16; ++i) w[i] = 0u;
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (out_dt == 1) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+}
+
+// Stores 32 packed outputs of one row at columns n0 .. n0 + 31 (those below N).
+__device__ __forceinline__ void store_packed_row32(uint8_t* dst_row, int32_t n0, int32_t N, int out_dt,
+                                                   const uint32_t (&w)[16], uint64_t pol) {
+  if (out_dt == 2) {
     uint8_t* dst = dst_row + n0;
     if (n0 + 32 <= N) {
       ptx::st_global_v4_hint(dst, w[0], w[1], w[2], w[3], pol);
@@ -213,46 +251,63 @@ __device__ __forceinline__ void store_row32(uint8_t* dst_row, int32_t n0, int32_
     }
     return;
   }
-  uint32_t packed[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if (out_dt == 1) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-      packed[i] = *reinterpret_cast<const uint32_t*>(&h);
-    } else {
-      const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
-      packed[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-  }
   uint16_t* dst = reinterpret_cast<uint16_t*>(dst_row) + n0;
   if (n0 + 32 <= N) {
 #pragma unroll
     for (int v = 0; v < 4; ++v)
-      ptx::st_global_v4_hint(reinterpret_cast<uint4*>(dst) + v, packed[4 * v], packed[4 * v + 1],
-                             packed[4 * v + 2], packed[4 * v + 3], pol);
+      ptx::st_global_v4_hint(reinterpret_cast<uint4*>(dst) + v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3],
+                             pol);
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (n0 + i < N) dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
+      if (n0 + i < N) dst[i] = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
   }
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW>
-__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THREADS, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>;
-  // Clusters of CS CTAs along M share each X panel: CTA rank r loads rows
+// Writes 32 packed outputs as row `lane` of a 32 x 32 staging box: 64-byte rows
+// with the 64B swizzle (fp16/bf16) or 32-byte rows with the 32B swizzle (e4m3),
+// the layouts the output tensor map stores from, without bank conflicts between
+// the lanes of a quarter warp.
+__device__ __forceinline__ void stage_packed_row32(uint8_t* buf, uint32_t lane, int out_dt, const uint32_t (&w)[16]) {
+  if (out_dt == 2) {
+    uint8_t* row = buf + lane * 32;
+#pragma unroll
+    for (int v = 0; v < 2; ++v)
+      *reinterpret_cast<uint4*>(row + ((v ^ ((lane >> 2) & 1)) << 4)) =
+          make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    return;
+  }
+  uint8_t* row = buf + lane * 64;
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    *reinterpret_cast<uint4*>(row + ((v ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+}
+
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR>
+__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>::THREADS, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+           const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY, const Params p) {
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>;
+  // Multicast clusters (CS CTAs along M) share each X panel: CTA rank r loads rows
   // [r BK/CS, (r+1) BK/CS) of every B box of a stage and multicasts them to the
   // whole cluster, so a stage is complete only when all CS slices have landed and
   // can be refilled only when all CS MMA issuers have released it.
-  const uint32_t crank = (CS > 1) ? ptx::cluster_ctarank() : 0u;
-  const int32_t unit0 = static_cast<int32_t>(blockIdx.x) / CS;
-  const int32_t unit_stride = static_cast<int32_t>(gridDim.x) / CS;
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CS) - 1u);
+  // SM pairs (PAIR): both CTAs load their own A rows, metadata and B columns, all
+  // counted on the even CTA's full barrier; the even CTA's MMA thread issues the
+  // M = 256 MMAs and its commits release both CTAs' stages and accumulators; the odd
+  // CTA's epilogue releases the accumulator on the even CTA's barrier.
+  constexpr int CL = C::CLUSTER;
+  const uint32_t crank = (CL > 1) ? ptx::cluster_ctarank() : 0u;
+  const bool leader = !PAIR || (crank & 1u) == 0u;
+  const int32_t unit0 = static_cast<int32_t>(blockIdx.x) / CL;
+  const int32_t unit_stride = static_cast<int32_t>(gridDim.x) / CL;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1u);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* staging = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STAGING_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* acc_full = bars + 2 * C::STAGES;
@@ -267,11 +322,11 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(&full[s], 1 + C::GATHER_THREADS);
-      ptx::mbar_init(&empty[s], CS);
+      ptx::mbar_init(&empty[s], C::MCAST ? CS : 1);
     }
     for (int a = 0; a < C::NACC; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], 128 * MT);
+      ptx::mbar_init(&acc_empty[a], 128 * MT * (PAIR ? 2 : 1));
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -280,13 +335,19 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    if constexpr (PAIR && SPARSE) ptx::prefetch_tmap(&tmM);
   }
   if (warp == 2) {
-    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  if constexpr (CS > 1)
+  if constexpr (CL > 1)
     ptx::cluster_sync();  // peers' barriers are initialised before any multicast reaches them
   else
     __syncthreads();
@@ -312,6 +373,20 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
         uint8_t* sB = sA + C::A_BYTES;
         uint8_t* sM = sB + C::B_BYTES;
         if (lane == 0) {
+          if constexpr (PAIR) {
+            // both CTAs' bytes complete on the even CTA's full barrier
+            constexpr uint32_t kTx = 2u * (C::A_BYTES + C::B_BYTES + (SPARSE ? 2048u : 0u));
+            if (leader) ptx::mbar_arrive_expect_tx(&full[stage], kTx);
+            const uint32_t bar = ptx::mapa(ptx::smem_u32(&full[stage]), crank & ~1u);
+            ptx::tma_load_2d_pair(sA, &tmA, bar, kb * (SPARSE ? C::BK / 2 : C::BK), ui.m0, pol_a);
+            if constexpr (SPARSE)  // one metadata block; past the last row block it reads zeros
+              ptx::tma_load_2d_pair(sM, &tmM, bar, 0, (ui.meta_blk0 + kb) * 16, pol_a);
+            const int32_t n_half = ui.n0 + static_cast<int32_t>(crank & 1u) * C::BN_CTA;
+#pragma unroll
+            for (int bx = 0; bx < C::B_BOXES; ++bx)
+              ptx::tma_load_2d_pair(sB + bx * C::B_BOX_BYTES, &tmB, bar, n_half + bx * C::B_BOX_COLS, kb * C::BK,
+                                    pol_b);
+          } else {
           ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0 : C::B_BYTES) +
                                                        (SPARSE ? 2048 * ui.subs : 0));
           // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
@@ -326,7 +401,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
             }
           }
           if constexpr (!GATHER) {
-            if constexpr (CS == 1) {
+            if constexpr (!C::MCAST) {
 #pragma unroll
               for (int bx = 0; bx < C::B_BOXES; ++bx)
                 ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS,
@@ -338,6 +413,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
                 ptx::tma_load_2d_multicast(sB + bx * C::B_BOX_BYTES + r0 * C::B_ROW, &tmB, &full[stage],
                                            ui.n0 + bx * C::B_BOX_COLS, kb * C::BK + r0, kMask, pol_b);
             }
+          }
           }
         }
         __syncwarp();
@@ -366,8 +442,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
         wait_bounded(&full[s], ph, nullptr);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------ MMA issuer
+    // (of an SM pair, only the even CTA issues)
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -396,8 +473,12 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
             meta_slot = (meta_slot + 1) % C::META_SLOTS;
             // per sub-tile: 128 rows x 16 B, rows contiguous (8-row core matrices 128 B apart)
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-              ptx::tmem_cp_128x128b(cur_meta + 4u * mt, ptx::sdesc(sM + 2048u * mt, 128, 128, 0));
+            for (int mt = 0; mt < MT; ++mt) {
+              if constexpr (PAIR)  // each CTA's block into its own TMEM
+                ptx::tmem_cp_128x128b_pair(cur_meta + 4u * mt, ptx::sdesc(sM + 2048u * mt, 128, 128, 0));
+              else
+                ptx::tmem_cp_128x128b(cur_meta + 4u * mt, ptx::sdesc(sM + 2048u * mt, 128, 128, 0));
+            }
           }
 #pragma unroll
           for (int j = 0; j < C::MMAS; ++j)
@@ -413,19 +494,29 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
               // (the sparse MMA reads it from an even column: one column for a
               // 16-bit K = 32 step, two for an e4m3 K = 64 step)
               const uint32_t col = 4u * mt + 2u * j;
-              if constexpr (C::F8)
+              if constexpr (PAIR && C::F8)
+                ptx::mma_sp_f8_pair(d_sub, adesc, bdesc, cur_meta + col, C::IDESC, accum);
+              else if constexpr (PAIR)
+                ptx::mma_sp_f16_pair(d_sub, adesc, bdesc, cur_meta + col, C::IDESC, accum);
+              else if constexpr (C::F8)
                 ptx::mma_sp_f8(d_sub, adesc, bdesc, cur_meta + col, C::IDESC, accum);
               else
                 ptx::mma_sp_f16(d_sub, adesc, bdesc, cur_meta + col, C::IDESC, accum);
             } else {
               const uint64_t adesc = ptx::sdesc(a_sub + j * 32, 16, 1024, 2);
-              if constexpr (C::F8)
+              if constexpr (PAIR && C::F8)
+                ptx::mma_f8_pair(d_sub, adesc, bdesc, C::IDESC, accum);
+              else if constexpr (PAIR)
+                ptx::mma_f16_pair(d_sub, adesc, bdesc, C::IDESC, accum);
+              else if constexpr (C::F8)
                 ptx::mma_f8(d_sub, adesc, bdesc, C::IDESC, accum);
               else
                 ptx::mma_f16(d_sub, adesc, bdesc, C::IDESC, accum);
             }
           }
-          if constexpr (CS > 1)
+          if constexpr (PAIR)
+            ptx::mma_commit_pair_multicast(&empty[stage], kMask);
+          else if constexpr (C::MCAST)
             ptx::mma_commit_multicast(&empty[stage], kMask);
           else
             ptx::mma_commit(&empty[stage]);
@@ -434,13 +525,21 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
         if (++stage == p.nstages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      if (lane == 0) ptx::mma_commit(&acc_full[acc]);
+      if (lane == 0) {
+        if constexpr (PAIR)
+          ptx::mma_commit_pair_multicast(&acc_full[acc], kMask);
+        else
+          ptx::mma_commit(&acc_full[acc]);
+      }
       __syncwarp();
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
     }
     // Make sure no MMA is still writing TMEM when the allocation is released.
     if (lane == 0) {
-      ptx::mma_commit(drain);
+      if constexpr (PAIR)
+        ptx::mma_commit_pair(drain);
+      else
+        ptx::mma_commit(drain);
       wait_bounded(drain, 0, nullptr);
     }
     __syncwarp();
@@ -517,6 +616,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
     const uint32_t q = warp & 3u;                 // TMEM lane quadrant this warp may read
     const uint32_t mt = (warp - 4u) >> 2;         // sub-tile this warp drains
     const uint64_t pol_y = ptx::policy_evict_first();  // the output is not re-read here
+    uint32_t chunk_seq = 0;                            // staging buffer alternation
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -530,8 +630,11 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
       uint8_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy * (p.out_dt == 2 ? 1 : 2);
       const bool has_bias = p.bias != nullptr;
       const float bias = (has_bias && row_ok) ? __ldg(p.bias + row) : 0.f;
+      constexpr int NCH = BN / 32;
+      const bool ragged_end = ((p.N * (p.out_dt == 2 ? 1 : 2)) & 15) != 0;
+      const int32_t wrow0 = ui.m0 + static_cast<int32_t>(128 * mt + 32 * q);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         uint32_t r[32];
         if (ui.nk > 0) {
           ptx::tmem_ld_32x32b_x32(
@@ -541,29 +644,67 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>::THR
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        if (c == BN / 32 - 1) {
+        if (c == NCH - 1) {  // the whole accumulator tile has been read: release it
           ptx::tc_fence_before();
-          ptx::mbar_arrive(&acc_empty[acc]);
+          if (leader)
+            ptx::mbar_arrive(&acc_empty[acc]);
+          else  // the odd CTA of a pair releases its rows on the even CTA's barrier
+            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&acc_empty[acc]), crank & ~1u));
         }
         const int32_t n0 = ui.n0 + 32 * c;
-        if (!row_ok || n0 >= p.N) continue;
         float x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, p.act, p.y_scale);
-        store_row32(yrow, n0, p.N, p.out_dt, x, pol_y);
+        uint32_t w[16];
+        pack_row32(p.out_dt, x, w);
+        if constexpr (C::STAGED) {
+          // this warp's 32 rows x 32 columns go through a staging buffer and a TMA
+          // store, which clips rows past M and columns past N
+          if (ui.phantom || wrow0 >= p.M || n0 >= p.N) continue;  // uniform over the warp
+          if (ragged_end && n0 + 32 > p.N) {
+            // a row end that is not a multiple of 16 bytes: the copy engine writes
+            // whole 16-byte units there, so that chunk is stored directly
+            if (row_ok) store_packed_row32(yrow, n0, p.N, p.out_dt, w, pol_y);
+            continue;
+          }
+          uint8_t* buf = staging + (warp - C::EPI_WARP0) * 4096 + (chunk_seq & 1) * 2048;
+          ++chunk_seq;
+          if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last used this buffer has read it
+          __syncwarp();
+          stage_packed_row32(buf, lane, p.out_dt, w);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmY, buf, n0, wrow0);
+            ptx::bulk_commit();
+          }
+        } else {
+          if (!row_ok || n0 >= p.N) continue;
+          store_packed_row32(yrow, n0, p.N, p.out_dt, w, pol_y);
+        }
       }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+    }
+    if constexpr (C::STAGED) {
+      if (lane == 0) ptx::bulk_wait<0>();  // this warp's output stores have completed
+      __syncwarp();
     }
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    ptx::cluster_sync();  // the even CTA's MMAs into both CTAs' TMEM have drained
+  else
+    __syncthreads();
   if (warp == 2) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if constexpr (CS > 1) ptx::cluster_sync();  // no CTA leaves while a peer may still signal it
+  if constexpr (C::MCAST) ptx::cluster_sync();  // no CTA leaves while a peer may still signal it
 }
 
 // ------------------------------------------------------------------ host side
@@ -606,11 +747,11 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128, bool PAIR = false>
 cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>;
   const int eb = C::EB;
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tM;
   bool ok;
   if constexpr (!GATHER) {
     if constexpr (SPARSE)
@@ -628,6 +769,23 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
       ok = make_map(&tA, a.A, eb, 64, a.packed_rows, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, 128 / eb, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  if constexpr (PAIR && SPARSE) {
+    // the 2048-byte metadata blocks as a (blocks * 16) x 128-byte matrix: one 16-row
+    // box per stage (long rows: the copy engine's cost grows with the rows of a box)
+    const uint64_t rows = static_cast<uint64_t>(ceil_div(a.M, 128)) * ceil_div(a.K, C::BK) * 16;
+    ok = ok && make_map(&tM, a.meta_hw, 1, 128, rows, 128, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    tM = tA;  // unused
+  }
+  CUtensorMap tY;
+  if constexpr (C::STAGED) {
+    // the output as 32 x 32 boxes (64-byte rows with the 64B swizzle; e4m3: 32-byte rows, 32B swizzle)
+    const bool f8_out = a.out_dt == SSDNN_E4M3;
+    ok = ok && make_map(&tY, a.Y, f8_out ? 1 : 2, a.N, a.M, a.ldy * (f8_out ? 1 : 2), 32, 32,
+                        f8_out ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+  } else {
+    tY = tA;  // unused
+  }
   if (!ok) return cudaErrorInvalidValue;
 
   Params p{};
@@ -636,7 +794,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.MB = static_cast<int32_t>(ceil_div(a.M, C::BM));
   p.MB128 = static_cast<int32_t>(ceil_div(a.M, 128));
   p.NB = static_cast<int32_t>(ceil_div(a.N, BN));
-  p.MG = static_cast<int32_t>(ceil_div(p.MB, CS));
+  p.MG = static_cast<int32_t>(ceil_div(p.MB, C::CLUSTER));
   {
     // bands of at most ~32 M groups, balanced
     const int64_t bands = ceil_div(p.MG, 32);
@@ -665,12 +823,13 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.err = err;
   if (p.num_units == 0) return cudaSuccess;
 
-  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW>;
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if constexpr (CS == 1) {
+  constexpr int CL = C::CLUSTER;
+  if constexpr (CL == 1) {
     const int grid = std::min(p.num_units, sm_count());
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, p);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, tM, tY, p);
     return cudaGetLastError();
   } else {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0)) != cudaSuccess)
@@ -678,7 +837,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -687,13 +846,13 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     // persistent: as many clusters as can be resident at once, at most one per work item
-    cfg.gridDim = dim3(static_cast<unsigned>(sm_count() / CS * CS), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count() / CL * CL), 1, 1);
     int max_clusters = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg)) != cudaSuccess) return e;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const int clusters = std::min(p.num_units, max_clusters);
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CS), 1, 1);
-    return cudaLaunchKernelEx(&cfg, kern, tA, tB, p);
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
+    return cudaLaunchKernelEx(&cfg, kern, tA, tB, tM, tY, p);
   }
 }
 
@@ -724,36 +883,39 @@ cudaError_t run_clustered(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
 // (sub-tiles of 128 rows, N tile).
 struct TileChoice {
   int mt, bn;
+  bool pair;  // an SM pair (two CTAs, M = 256 MMAs) per 256 x bn tile
 };
 TileChoice choose_tile(bool sparse, int eb, int64_t M, int64_t N) {
   // 16-bit inputs also have 128x64 tiles, which give small-M shapes (a BERT FFN
   // down projection: 768 rows) twice the work units of 128x128
-  const TileChoice dense_c[] = {{1, 64}, {1, 128}, {1, 256}, {2, 256}};
-  const TileChoice sp16_c[] = {{1, 64}, {1, 128}, {1, 256}, {2, 192}};
+  // dense: large problems run on SM pairs (256 x 256 tiles, double-buffered accumulator)
+  const TileChoice dense_c[] = {{1, 64, false}, {1, 128, false}, {1, 256, false}, {1, 256, true}};
+  const TileChoice sp16_c[] = {{1, 64, false}, {1, 128, false}, {1, 256, false}, {2, 192, false}};
   // e4m3 2:4: 256x192 tiles (64-byte B boxes); 256x128 measured slower than 128x256
-  const TileChoice sp8_c[] = {{1, 128}, {1, 128}, {1, 256}, {2, 192}};
-  const TileChoice dense8_c[] = {{1, 128}, {1, 128}, {1, 256}, {2, 256}};
+  const TileChoice sp8_c[] = {{1, 128, false}, {1, 128, false}, {1, 256, false}, {2, 192, false}};
+  const TileChoice dense8_c[] = {{1, 128, false}, {1, 128, false}, {1, 256, false}, {1, 256, true}};
   const TileChoice* cand = !sparse ? (eb == 2 ? dense_c : dense8_c) : (eb == 2 ? sp16_c : sp8_c);
   const int64_t sms = sm_count();
   TileChoice best = cand[0];
   double best_cost = 1e300;
   for (int i = 0; i < 4; ++i) {
     const TileChoice c = cand[i];
-    const int64_t units = ceil_div(M, 128 * c.mt) * ceil_div(N, c.bn);
+    // an SM pair covers 256 rows with two CTAs, each filling 128 rows and half of the X panel
+    const int64_t units = ceil_div(M, c.pair ? 256 : 128 * c.mt) * ceil_div(N, c.bn) * (c.pair ? 2 : 1);
     const int64_t waves = ceil_div(units, sms);
-    const int64_t stage = c.mt * (sparse ? 8192 + 2048 : 16384) + 128 * c.bn;
-    const double cost = static_cast<double>(waves) * static_cast<double>(stage) * (1.0 + 0.02 * c.mt);
+    const int64_t stage = c.pair ? (sparse ? 8192 + 2048 : 16384) + 64 * c.bn
+                                 : c.mt * (sparse ? 8192 + 2048 : 16384) + 128 * c.bn;
+    const double cost = static_cast<double>(waves) * static_cast<double>(stage) * (1.0 + 0.02 * (c.pair ? 2 : c.mt));
     if (cost < best_cost) { best_cost = cost; best = c; }
   }
   return best;
 }
 
+// Tuning override, read at each call: SSDNN_TILE = MT * 1000 + BN (e.g. 2192), or
+// 9000 + BN for an SM-pair tile (e.g. 9256).
 int tile_override() {
-  static int v = [] {
-    const char* e = getenv("SSDNN_TILE");  // "MT*1000 + BN", e.g. 2192
-    return e ? atoi(e) : 0;
-  }();
-  return v;
+  const char* e = getenv("SSDNN_TILE");
+  return e ? atoi(e) : 0;
 }
 
 template <int DT>
@@ -762,7 +924,17 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
   if (mode == 0 || mode == 1) {
     const bool sparse = mode == 1;
     TileChoice c = choose_tile(sparse, EB, a.M, a.N);
-    if (tile_override()) c = TileChoice{tile_override() / 1000, tile_override() % 1000};
+    if (const int ov = tile_override()) c = TileChoice{ov / 1000 == 9 ? 1 : ov / 1000, ov % 1000, ov / 1000 == 9};
+    if (c.pair && sparse) {
+      // the metadata tensor map addresses 128-row blocks by an int32 row coordinate
+      const int64_t meta_rows = ceil_div(a.M, 128) * ceil_div(a.K, 128 / EB) * 16;
+      if (meta_rows > INT32_MAX) c = TileChoice{2, 192, false};
+    }
+    if (c.pair) {
+      if (c.bn != 256) return cudaErrorInvalidValue;
+      return sparse ? run<DT, true, false, 256, 1, 1, 128, true>(a, s, err)
+                    : run<DT, false, false, 256, 1, 1, 128, true>(a, s, err);
+    }
     if (c.mt == 2) {
       if (!sparse && c.bn == 256) return run<DT, false, false, 256, 1, 2>(a, s, err);
       if (sparse && EB == 2 && c.bn == 192) {

@@ -178,3 +178,47 @@ def test_mma_rate_microbenchmark_runs_clean(dt, sparse):
         ss.mma_rate(ss.BF16 if dt == "bf16" else ss.E4M3, sparse, n, 64)
     torch.cuda.synchronize()
     assert ss.check_device_error() == 0
+
+
+# Every tile variant, forced through the tile override (MT * 1000 + BN; 9000 + BN
+# for an SM pair: two CTAs of a cluster run M = 256 MMAs, each holding 128 rows of
+# W and half of the X panel), on a shape with ragged M (the odd CTA of the last
+# pair has no rows), ragged N and a partial last K stage, and on a multi-wave shape.
+FORCED_SHAPES = [(300, 264, 520), (2000, 8192, 256)]
+
+
+def _forced_tiles(dt, sparse):
+    tiles = ["1128", "1256", "9256"] + (["1064"] if dt != "e4m3" else [])
+    return tiles + (["2192"] if sparse else ["2256"])
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("shape", FORCED_SHAPES)
+@pytest.mark.parametrize("sparse", [True, False])
+def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
+    ss = lib()
+    M, N, K = shape
+    W = rand_bits(700 + M, (M, K), dt, 0.5)
+    X = rand_bits(710 + N, (K, N), dt, 1.0)
+    out_dt = "bf16" if dt == "e4m3" else dt
+    alpha = 0.75 if dt == "e4m3" else 1.0
+    if sparse:
+        v_ref, m_ref = oracle.sp24.compress(W, dt)
+        Y_ref = oracle.gemm.gemm_sp24(v_ref, m_ref, K, X, dt, out_dt, alpha)
+        B = oracle.gemm.bound(oracle.sp24.decompress(v_ref, m_ref, K), X, dt, alpha)
+        f = ss.sp24_prune_compress(dev_tensor(W, dt), canonical_meta=False)
+    else:
+        Y_ref = oracle.gemm.gemm_dense(W, X, dt, out_dt, alpha)
+        B = oracle.gemm.bound(W, X, dt, alpha)
+    Xd = dev_padded(X, dt)
+    for tile in _forced_tiles(dt, sparse):
+        monkeypatch.setenv("SSDNN_TILE", tile)
+        Y, buf = guarded_output(M, N, torch.bfloat16 if out_dt == "bf16" else torch.float16)
+        if sparse:
+            ss.sp24_gemm(f, Xd, alpha=alpha, out=Y)
+        else:
+            ss.dense_gemm(dev_padded(W, dt), Xd, alpha=alpha, out=Y)
+        torch.cuda.synchronize()
+        assert ss.check_device_error() == 0, tile
+        _check_y(Y, Y_ref, B, out_dt, REL[dt])
+        assert canary_intact(buf, M, N), tile
