@@ -86,9 +86,13 @@ struct Cfg {
   // 4 control warps, 4 epilogue warps per sub-tile, and for TW/TVW 4 warps that
   // gather the kept X rows with 16-byte cp.async
   static constexpr int GATHER_THREADS = GATHER ? 128 : 0;
+  // SM pairs drain their 128 x 256 accumulator with eight epilogue warps (two per
+  // TMEM lane quadrant, each taking half of the columns)
+  static constexpr int EPI_SPLIT = PAIR ? 2 : 1;
+  static constexpr int EPI_WARPS = 4 * MT * EPI_SPLIT;
   static constexpr int EPI_WARP0 = 4;
-  static constexpr int GATHER_WARP0 = 4 + 4 * MT;
-  static constexpr int THREADS = 128 + 128 * MT + GATHER_THREADS;
+  static constexpr int GATHER_WARP0 = 4 + EPI_WARPS;
+  static constexpr int THREADS = 128 + 32 * EPI_WARPS + GATHER_THREADS;
   static constexpr int STAGES_FOR_LAG = ((220 * 1024) / (MT * (SPARSE ? 128 * 64 : 128 * 128) + 128 * BN +
                                                            (SPARSE ? 2048 * MT : 0)));
   // stages a gather thread keeps in flight before it must see its oldest copies land
@@ -106,7 +110,7 @@ struct Cfg {
   // into one of two 2 KB shared-memory buffers and a TMA store writes it out, so
   // the accumulator is drained without waiting on global stores.
   static constexpr bool STAGED = !GATHER;
-  static constexpr int STAGING_BYTES = STAGED ? 4 * MT * 4096 : 0;
+  static constexpr int STAGING_BYTES = STAGED ? EPI_WARPS * 4096 : 0;
   static constexpr int STAGES_RAW = (220 * 1024 - STAGING_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int MMA_K = (SPARSE ? 64 : 32) / EB;      // dense K per instruction
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     }
     for (int a = 0; a < C::NACC; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], 128 * MT * (PAIR ? 2 : 1));
+      ptx::mbar_init(&acc_empty[a], 32 * C::EPI_WARPS * (PAIR ? 2 : 1));
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -611,10 +615,11 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     ptx::cp_async_wait<0>();
     ptx::fence_proxy_async_smem();
     for (int d = 0; d < pending; ++d) ptx::mbar_arrive(&full[lag_stage[d]]);
-  } else if (warp >= C::EPI_WARP0 && warp < C::EPI_WARP0 + 4 * MT) {
+  } else if (warp >= C::EPI_WARP0 && warp < C::EPI_WARP0 + C::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp & 3u;                 // TMEM lane quadrant this warp may read
-    const uint32_t mt = (warp - 4u) >> 2;         // sub-tile this warp drains
+    const uint32_t mt = PAIR ? 0u : (warp - 4u) >> 2;  // sub-tile this warp drains
+    const int half = PAIR ? static_cast<int>((warp - 4u) >> 2) : 0;  // column half (SM pairs)
     const uint64_t pol_y = ptx::policy_evict_first();  // the output is not re-read here
     uint32_t chunk_seq = 0;                            // staging buffer alternation
     int acc = 0;
@@ -630,11 +635,12 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
       uint8_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy * (p.out_dt == 2 ? 1 : 2);
       const bool has_bias = p.bias != nullptr;
       const float bias = (has_bias && row_ok) ? __ldg(p.bias + row) : 0.f;
-      constexpr int NCH = BN / 32;
+      constexpr int NCH = BN / 32 / C::EPI_SPLIT;   // 32-column chunks this warp drains
+      const int c0 = half * NCH;
       const bool ragged_end = ((p.N * (p.out_dt == 2 ? 1 : 2)) & 15) != 0;
       const int32_t wrow0 = ui.m0 + static_cast<int32_t>(128 * mt + 32 * q);
 #pragma unroll 1
-      for (int c = 0; c < NCH; ++c) {
+      for (int c = c0; c < c0 + NCH; ++c) {
         uint32_t r[32];
         if (ui.nk > 0) {
           ptx::tmem_ld_32x32b_x32(
@@ -644,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        if (c == NCH - 1) {  // the whole accumulator tile has been read: release it
+        if (c == c0 + NCH - 1) {  // this warp's part of the accumulator has been read: release it
           ptx::tc_fence_before();
           if (leader)
             ptx::mbar_arrive(&acc_empty[acc]);
@@ -891,8 +897,9 @@ TileChoice choose_tile(bool sparse, int eb, int64_t M, int64_t N) {
   // dense: large problems run on SM pairs (256 x 256 tiles, double-buffered accumulator)
   const TileChoice dense_c[] = {{1, 64, false}, {1, 128, false}, {1, 256, false}, {1, 256, true}};
   const TileChoice sp16_c[] = {{1, 64, false}, {1, 128, false}, {1, 256, false}, {2, 192, false}};
-  // e4m3 2:4: 256x192 tiles (64-byte B boxes); 256x128 measured slower than 128x256
-  const TileChoice sp8_c[] = {{1, 128, false}, {1, 128, false}, {1, 256, false}, {2, 192, false}};
+  // e4m3 2:4: SM-pair 256x256 tiles for large problems (measured ahead of 256x192
+  // tiles with 64-byte B boxes, which stay ahead for fp16/bf16)
+  const TileChoice sp8_c[] = {{1, 128, false}, {1, 256, false}, {2, 192, false}, {1, 256, true}};
   const TileChoice dense8_c[] = {{1, 128, false}, {1, 128, false}, {1, 256, false}, {1, 256, true}};
   const TileChoice* cand = !sparse ? (eb == 2 ? dense_c : dense8_c) : (eb == 2 ? sp16_c : sp8_c);
   const int64_t sms = sm_count();
