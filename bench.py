@@ -154,6 +154,9 @@ def timed_steps(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> lis
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    # keep the GPU busy while the host enqueues the first steps, so that no step's
+    # events include host launch latency
+    torch.cuda._sleep(2_000_000)
     evs = []
     for _ in range(steps):
         flush.fill_(1)
@@ -260,10 +263,13 @@ def run_gpu(args) -> None:
     X_host = I.torch_view(d["X"], wl.dt).pin_memory()
     Y_host = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
 
+    # the library's host-buffer call: X copied in, then Y computed in row blocks,
+    # each block copied out on a second stream while the next one is computed
+    copy_stream = torch.cuda.Stream(device=dev)
+    e2e_rows = 2048
+
     def e2e_step():
-        Xd.copy_(X_host, non_blocking=True)
-        step()
-        Y_host.copy_(Y, non_blocking=True)
+        ss.sp24_gemm_host(form, X_host, Y_host, Xd, Y, alpha=alpha, rows_per_block=e2e_rows, copy_stream=copy_stream)
 
     e2e_times = timed_steps(e2e_step, max(3, args.steps // 2), 2, flush, stream)
     e2e_value = ws * eff_flops / (statistics.mean(e2e_times) * 1e-3) / 1e12
@@ -293,6 +299,7 @@ def run_gpu(args) -> None:
                                       f"{'2 x ' if wl.dt == 'e4m3' else ''}{pk['source']} bf16 dense burst "
                                       f"{pk['bf16_tflops']}"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                    "path": f"sp24_gemm_host (pinned host X and Y, {e2e_rows}-row blocks, copies overlapped)",
                     "h2d_bytes_per_step": int(Xd.numel() * Xd.element_size()),
                     "d2h_bytes_per_step": int(Y.numel() * Y.element_size())},
             "mma_microbench_dense_equivalent_tflops": mma,

@@ -173,6 +173,20 @@ int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* ke
              const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
              const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream);
 
+/* sp24_gemm with the activations and the result in host memory. X_host (K x N,
+ * pitch ldx) is copied to the caller's device buffer X_dev (same pitch) on
+ * `stream`; Y is computed into the caller's device buffer Y_dev (M x N, pitch ldy)
+ * in blocks of rows_per_block rows (a multiple of 128; 0 = one block), and each
+ * block is copied to Y_host (pitch ldy) on `copy_stream` as soon as its GEMM has
+ * finished, while the next block is computed (copy_stream NULL: everything runs
+ * on `stream`, in order). The host buffers should be page-locked for the copies
+ * to be asynchronous. The call only enqueues; Y_host is complete once `stream`
+ * has completed. Returns as sp24_gemm, or SSDNN_ERR_INVALID_ARG for a null host
+ * buffer or a block height that is not a multiple of 128. */
+int sp24_gemm_host(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+                   const uint8_t* meta_hw, const void* X_host, int64_t ldx, void* Y_host, int64_t ldy, float alpha,
+                   void* X_dev, void* Y_dev, int64_t rows_per_block, void* stream, void* copy_stream);
+
 /* --------------------------------------------------- fused layer epilogue ----
  * A pruned fully connected layer or 1x1 convolution runs as one of the GEMMs
  * above ("Accelerating Sparse DNNs Based on Tiled GEMM", Abstract), and the step

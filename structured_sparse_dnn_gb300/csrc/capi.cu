@@ -45,6 +45,22 @@ __global__ void k_selftest_timeout(uint32_t* err, uint64_t limit_ns) {
   wait_bounded(&bar, 0, err, limit_ns);
 }
 
+// Ordering events for the host-buffer GEMM: a small per-device pool, created on
+// first use and reused (re-recording an event is safe once waits have been
+// enqueued against its previous record). Index -1 is the completion event.
+constexpr int kCopyEvents = 64;
+cudaEvent_t g_events[kMaxDevices][kCopyEvents + 1] = {};
+
+cudaEvent_t copy_event(int64_t i) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const int slot = i < 0 ? kCopyEvents : static_cast<int>(i % kCopyEvents);
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  cudaEvent_t& e = g_events[dev][slot];
+  if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) e = nullptr;
+  return e;
+}
+
 int elem_bytes(int dt) { return dt == SSDNN_E4M3 ? 1 : 2; }
 bool valid_dt(int dt) { return dt == SSDNN_F16 || dt == SSDNN_BF16 || dt == SSDNN_E4M3; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -329,6 +345,54 @@ int sp24_gemm_ep(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const v
                  const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
                  const ssdnn_epilogue* ep, void* stream) {
   return sp24_gemm_impl(in_dt, out_dt, M, N, K, values, meta_hw, X, ldx, Y, ldy, alpha, ep, true, stream);
+}
+
+int sp24_gemm_host(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+                   const uint8_t* meta_hw, const void* X_host, int64_t ldx, void* Y_host, int64_t ldy, float alpha,
+                   void* X_dev, void* Y_dev, int64_t rows_per_block, void* stream, void* copy_stream) {
+  if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
+  const int eb = elem_bytes(in_dt);
+  int st = check_gemm_io(out_dt, false, M, N, K, X_dev, ldx, eb, Y_dev, ldy);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (!Y_host || (K > 0 && !X_host)) return SSDNN_ERR_INVALID_ARG;
+  if (rows_per_block < 0 || rows_per_block % 128) return SSDNN_ERR_INVALID_ARG;
+  if (K % 4) return SSDNN_ERR_UNSUPPORTED;
+  auto s = static_cast<cudaStream_t>(stream);
+  auto cs = copy_stream ? static_cast<cudaStream_t>(copy_stream) : s;
+  const int ob = out_bytes(out_dt);
+  const size_t y_pitch = static_cast<size_t>(ldy * ob);
+  if (K > 0) {
+    const size_t x_pitch = static_cast<size_t>(ldx * eb);
+    if (cudaMemcpy2DAsync(X_dev, x_pitch, X_host, x_pitch, static_cast<size_t>(N * eb), static_cast<size_t>(K),
+                          cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return SSDNN_ERR_CUDA;
+  }
+  const int64_t rb = rows_per_block > 0 ? rows_per_block : M;
+  const int64_t Kp = round_up(K, 32), KB = ceil_div(K, in_dt == SSDNN_E4M3 ? 128 : 64);
+  for (int64_t r0 = 0; r0 < M; r0 += rb) {
+    const int64_t rows = std::min(rb, M - r0);
+    const auto* vals = static_cast<const uint8_t*>(values) + r0 * (Kp / 2) * eb;
+    const uint8_t* meta = meta_hw + (r0 / 128) * KB * 2048;
+    uint8_t* yd = static_cast<uint8_t*>(Y_dev) + r0 * ldy * ob;
+    st = sp24_gemm_impl(in_dt, out_dt, rows, N, K, K > 0 ? vals : nullptr, K > 0 ? meta : nullptr, X_dev, ldx, yd, ldy,
+                        alpha, nullptr, false, stream);
+    if (st != SSDNN_OK) return st;
+    if (cs != s) {  // the copy stream takes this block as soon as its GEMM has finished
+      cudaEvent_t ev = copy_event(r0 / rb);
+      if (!ev || cudaEventRecord(ev, s) != cudaSuccess || cudaStreamWaitEvent(cs, ev, 0) != cudaSuccess)
+        return SSDNN_ERR_CUDA;
+    }
+    if (cudaMemcpy2DAsync(static_cast<uint8_t*>(Y_host) + r0 * y_pitch, y_pitch, yd, y_pitch,
+                          static_cast<size_t>(N * ob), static_cast<size_t>(rows), cudaMemcpyDeviceToHost,
+                          cs) != cudaSuccess)
+      return SSDNN_ERR_CUDA;
+  }
+  if (cs != s) {  // the caller's stream completes only after the last copy
+    cudaEvent_t ev = copy_event(-1);
+    if (!ev || cudaEventRecord(ev, cs) != cudaSuccess || cudaStreamWaitEvent(s, ev, 0) != cudaSuccess)
+      return SSDNN_ERR_CUDA;
+  }
+  return SSDNN_OK;
 }
 
 int dense_gemm(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,

@@ -113,3 +113,6 @@ def test_argument_errors_before_any_device_work(ssdnn):
     assert lib.sp24_gemm_ep(0, 0, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, C.byref(ep), None) == 2
     assert lib.sp24_gemm_ep(0, 2, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, None, None) == 2      # e4m3 row pitch 8 B
     assert lib.sp24_gemm(0, 2, 4, 16, 8, 16, 16, 16, 16, 16, 16, 1.0, None) == 2          # plain call: no e4m3 out
+    # the host-buffer GEMM: block height a multiple of 128, host buffers required
+    assert lib.sp24_gemm_host(1, 1, 256, 8, 64, 16, 16, 16, 8, 16, 8, 1.0, 16, 16, 100, None, None) == 1
+    assert lib.sp24_gemm_host(1, 1, 256, 8, 64, 16, 16, None, 8, 16, 8, 1.0, 16, 16, 128, None, None) == 1

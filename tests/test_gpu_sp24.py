@@ -222,3 +222,27 @@ def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
         assert ss.check_device_error() == 0, tile
         _check_y(Y, Y_ref, B, out_dt, REL[dt])
         assert canary_intact(buf, M, N), tile
+
+
+@pytest.mark.parametrize("copy_stream", [False, True])
+@pytest.mark.parametrize("rows_per_block", [0, 256])
+def test_sp24_gemm_host_buffers(copy_stream, rows_per_block):
+    """The host-buffer form: X copied in from pinned memory, Y computed in row
+    blocks and copied out (overlapped on a second stream), against the oracle."""
+    ss = lib()
+    M, N, K, dt = 1000, 264, 520, "bf16"
+    W = rand_bits(801, (M, K), dt, 0.5)
+    X = rand_bits(802, (K, N), dt, 1.0)
+    f = ss.sp24_prune_compress(dev_tensor(W, dt), canonical_meta=False)
+    X_host = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Y_host = torch.full((M, N), 7.0, dtype=torch.bfloat16).pin_memory()
+    X_dev = torch.empty((K, N), dtype=torch.bfloat16, device="cuda")
+    Y_dev = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    cs = torch.cuda.Stream() if copy_stream else None
+    ss.sp24_gemm_host(f, X_host, Y_host, X_dev, Y_dev, rows_per_block=rows_per_block, copy_stream=cs)
+    torch.cuda.current_stream().synchronize()
+    assert ss.check_device_error() == 0
+    v_ref, m_ref = oracle.sp24.compress(W, dt)
+    Y_ref = oracle.gemm.gemm_sp24(v_ref, m_ref, K, X, dt, dt)
+    B = oracle.gemm.bound(oracle.sp24.decompress(v_ref, m_ref, K), X, dt)
+    _check_y(Y_host, Y_ref, B, dt, REL[dt])
