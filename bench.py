@@ -154,9 +154,10 @@ def timed_steps(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> lis
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    # keep the GPU busy while the host enqueues the first steps, so that no step's
-    # events include host launch latency
-    torch.cuda._sleep(2_000_000)
+    # an untimed lead-in step keeps every SM busy (and the clocks up) while the host
+    # enqueues the first timed steps, so that no step's events include launch latency
+    flush.fill_(1)
+    fn()
     evs = []
     for _ in range(steps):
         flush.fill_(1)
@@ -290,6 +291,8 @@ def run_gpu(args) -> None:
                                    f"{wl.dt} in, {wl.out_dt} out, fp32 accumulate",
                        "M": M, "K": K, "N": N, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "l2": "flushed between timed steps (256 MB write)"},
+            "step_ms": {"min": round(min(times), 5), "median": round(statistics.median(times), 5),
+                        "max": round(max(times), 5)},
             "pct_of_sparse_peak": round(100.0 * achieved / peak_eff, 2),
             "dense_equivalent_tflops": round(2 * achieved, 2),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak_eff, 1),
