@@ -431,6 +431,15 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
     t_tw = statistics.mean(timed_steps(lambda: ss.tvw_gemm(form_tw, Xt, out=Yt), steps, 2, flush, stream))
     t_tvw = statistics.mean(timed_steps(lambda: ss.tvw_gemm(form_tvw, Xt, out=Yt), steps, 2, flush, stream))
     t_dense = statistics.mean(timed_steps(lambda: ss.dense_gemm(Wt, Xt, out=Yt), steps, 2, flush, stream))
+    # block-wise (NEXT-2) at the same per-tile kept fractions: 64-column blocks
+    keep_b = (keep // 64).astype(np.int32)
+    szb = ss.bw_sizes(ss.BF16, tw.M, tw.K, keep_b)
+    work_b = torch.empty(szb["workspace_bytes"], dtype=torch.uint8, device=dev)
+    t_bw_prune = statistics.mean(timed_steps(lambda: ss.bw_prune_compress(Wt, keep_b, work_b), steps, 2, flush,
+                                             stream))
+    form_bw = ss.bw_prune_compress(Wt, keep_b, work_b)
+    t_bw = statistics.mean(timed_steps(lambda: ss.bw_gemm(form_bw, Xt, out=Yt), steps, 2, flush, stream))
+    flops_bw = 2.0 * 128 * 64 * float(keep_b.sum()) * tw.N
     dens = 128.0 * keep.sum() / (tw.M * tw.K)
     flops_tw = 2.0 * 128 * float(keep.sum()) * tw.N
     flops_tvw = 2.0 * 128 * float(keep4.sum()) * tw.N * 0.5
@@ -442,6 +451,10 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
         "dense_gemm_ms": round(t_dense, 4),
         "dense_TFLOP/s": round(2.0 * tw.M * tw.N * tw.K / (t_dense * 1e-3) / 1e12, 1),
         "tvw_speedup_over_dense": round(t_dense / t_tvw, 3), "tw_speedup_over_dense": round(t_dense / t_tw, 3),
+        "bw_prune_compress_ms": round(t_bw_prune, 4), "bw_gemm_ms": round(t_bw, 4),
+        "bw_effective_TFLOP/s": round(flops_bw / (t_bw * 1e-3) / 1e12, 1),
+        "bw_kept_fraction": round(float(keep_b.sum()) * 64 / tw.K / len(keep_b), 4),
+        "bw_speedup_over_dense": round(t_dense / t_bw, 3),
         "sparsity": round(1 - float(dens), 4),
     }
     return rows

@@ -187,6 +187,36 @@ int sp24_gemm_host(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const
                    const uint8_t* meta_hw, const void* X_host, int64_t ldx, void* Y_host, int64_t ldy, float alpha,
                    void* X_dev, void* Y_dev, int64_t rows_per_block, void* stream, void* copy_stream);
 
+/* ------------------------------------------------------------ block-wise ----
+ * Block sparsity, the comparison pattern of the tiled-GEMM page ("Accelerating
+ * Sparse DNNs Based on Tiled GEMM", Abstract; Figure 5 caption: BW pruning):
+ * whole blocks of W are removed. Readings (the page fixes no block shape): a
+ * block is 128 rows (one tile, as for TW) x 64 consecutive columns; K % 64 == 0.
+ * Block score = fp32 sum over the block's 64 columns, ascending, of the TW
+ * column scores (fp32 sums of |w| over the tile's rows, ascending); tile t keeps
+ * the first keep_blocks_host[t] blocks of (score descending, block ascending),
+ * listed ascending. The GEMM reads each kept block's 64-row X panel with one TMA
+ * box (no gather).
+ * Layouts (nt = ceil(M / 128), B_t = keep_blocks_host[t], P_t = sum_{s<t} 64 B_s):
+ *   offsets   nt + 1 int32, offsets[t] = sum_{s<t} B_s (in blocks).
+ *   indices   sum B_t int32: the kept block indices of each tile, ascending.
+ *   schedule  4 nt int32: (t, 64 B_t, P_t, P_t / 64), tiles by B_t descending, as TW.
+ *   packed    the TW dense packed operand of the kept columns: element (t, r, j),
+ *             j < 64 B_t, at 128 P_t + 8192 (j / 64) + 64 r + j % 64 (rows past M zero).
+ *   workspace bw_sizes' workspace_bytes (scores and column lists).
+ * fp16/bf16 only (E4M3: SSDNN_ERR_UNSUPPORTED); K % 64 != 0: SSDNN_ERR_UNSUPPORTED. */
+int bw_sizes(int dt, int64_t M, int64_t K, const int32_t* keep_blocks_host, size_t* packed_bytes,
+             size_t* indices_count, size_t* workspace_bytes);
+int bw_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, const int32_t* keep_blocks_host,
+                      int32_t* offsets, int32_t* indices, int32_t* schedule, void* packed, void* workspace,
+                      void* stream);
+/* Y[tile t] = W_t . X[kept rows], fp32 accumulation, one RNE conversion to dt; a
+ * tile that keeps no block writes zeros. bw_gemm_ep adds the output type, alpha
+ * and the fused epilogue (below). */
+int bw_gemm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* keep_blocks_host, const int32_t* offsets,
+            const int32_t* indices, const int32_t* schedule, const void* packed, const void* X, int64_t ldx, void* Y,
+            int64_t ldy, void* stream);
+
 /* --------------------------------------------------- fused layer epilogue ----
  * A pruned fully connected layer or 1x1 convolution runs as one of the GEMMs
  * above ("Accelerating Sparse DNNs Based on Tiled GEMM", Abstract), and the step
@@ -207,7 +237,7 @@ typedef struct ssdnn_epilogue {
   float y_scale;     /* finite multiplier after the activation (1.0f = none) */
 } ssdnn_epilogue;
 
-/* sp24_gemm / dense_gemm / tvw_gemm with the fused epilogue `ep` (NULL = the
+/* sp24_gemm / dense_gemm / tvw_gemm / bw_gemm with the fused epilogue `ep` (NULL = the
  * plain conversion). out_dt may also be SSDNN_E4M3 here (ldy * out bytes a
  * multiple of 16). Returns SSDNN_ERR_INVALID_ARG for an unknown activation or a
  * non-finite y_scale, SSDNN_ERR_UNSUPPORTED for a misaligned bias; otherwise as
@@ -223,6 +253,10 @@ int tvw_gemm_ep(int dt, int out_dt, int tvw, int64_t M, int64_t N, int64_t K, co
                 const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
                 const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
                 const ssdnn_epilogue* ep, void* stream);
+int bw_gemm_ep(int dt, int out_dt, int64_t M, int64_t N, int64_t K, const int32_t* keep_blocks_host,
+               const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+               const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+               void* stream);
 
 /* ------------------------------------------------- allocation-free variant ----
  * tw_prune_compress_noalloc: tw_prune_compress for callers that cannot allocate

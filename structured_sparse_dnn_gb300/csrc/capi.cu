@@ -159,6 +159,40 @@ int build_tables(int tvw, int64_t M, int64_t K, const int32_t* keep, Tables* out
   return SSDNN_OK;
 }
 
+// Block-wise tables: per-tile kept block counts -> the tile-wise tables of the kept
+// columns (L_t = 64 B_t) plus the block offsets, and the workspace layout.
+struct BwTables {
+  Tables cols;                      // tile-wise tables of the kept columns
+  std::vector<int32_t> blk_offsets;  // nt + 1, in blocks
+  int64_t n_blocks = 0;
+  size_t ws_scores = 0, ws_bscores = 0, ws_coloff = 0, ws_colidx = 0, ws_bytes = 0;  // byte offsets
+};
+
+int build_bw_tables(int64_t M, int64_t K, const int32_t* keep_blocks, BwTables* out) {
+  if (K % 64) return SSDNN_ERR_UNSUPPORTED;
+  const int64_t nt = ceil_div(M, 128), KB = K / 64;
+  std::vector<int32_t> keep_cols(static_cast<size_t>(nt));
+  out->blk_offsets.assign(static_cast<size_t>(nt + 1), 0);
+  int64_t nb = 0;
+  for (int64_t t = 0; t < nt; ++t) {
+    const int64_t b = keep_blocks[t];
+    if (b < 0 || b > KB) return SSDNN_ERR_INVALID_ARG;
+    keep_cols[static_cast<size_t>(t)] = static_cast<int32_t>(64 * b);
+    nb += b;
+    out->blk_offsets[static_cast<size_t>(t + 1)] = static_cast<int32_t>(nb);
+  }
+  out->n_blocks = nb;
+  const int st = build_tables(0, M, K, keep_cols.data(), &out->cols);
+  if (st != SSDNN_OK) return st;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  out->ws_scores = 0;
+  out->ws_bscores = up(static_cast<size_t>(nt * K) * 4);
+  out->ws_coloff = out->ws_bscores + up(static_cast<size_t>(nt * KB) * 4);
+  out->ws_colidx = out->ws_coloff + up(static_cast<size_t>(nt + 1) * 4);
+  out->ws_bytes = out->ws_colidx + up(static_cast<size_t>(64 * nb) * 4);
+  return SSDNN_OK;
+}
+
 }  // namespace
 int sp24_gemm_impl(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
                    const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
@@ -256,6 +290,43 @@ int tvw_gemm_impl(int dt, int out_dt, int tvw, int64_t M, int64_t N, int64_t K, 
   a.schedule = schedule;
   set_epilogue(a, ep);
   return from_cuda(launch_gemm(tvw ? 3 : 2, a, s, error_word()));
+}
+
+int bw_gemm_impl(int dt, int out_dt, int64_t M, int64_t N, int64_t K, const int32_t* keep_blocks_host,
+                 const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+                 const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+                 bool f8_out_ok, void* stream) {
+  if (dt != SSDNN_F16 && dt != SSDNN_BF16) return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  int st = check_gemm_io(out_dt, f8_out_ok, M, N, K, X, ldx, 2, Y, ldy);
+  if (st == SSDNN_OK) st = check_epilogue(ep);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (!keep_blocks_host) return SSDNN_ERR_INVALID_ARG;
+  BwTables tb;
+  st = build_bw_tables(M, K, keep_blocks_host, &tb);
+  if (st != SSDNN_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0 || tb.n_blocks == 0) return empty_product(Y, ldy, M, N, out_dt, ep, s);
+  if (!offsets || !indices || !schedule || !packed) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = packed;
+  a.X = X;
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  a.nt = tb.cols.t.nt;
+  a.packed_rows = 2 * tb.cols.t.P_total;
+  a.offsets = offsets;
+  a.indices = indices;
+  a.schedule = schedule;
+  set_epilogue(a, ep);
+  return from_cuda(launch_gemm(4, a, s, error_word()));
 }
 
 }  // namespace ssdnn
@@ -466,6 +537,71 @@ int tvw_gemm_ep(int dt, int out_dt, int tvw, int64_t M, int64_t N, int64_t K, co
                 const ssdnn_epilogue* ep, void* stream) {
   return tvw_gemm_impl(dt, out_dt, tvw, M, N, K, keep_counts_host, offsets, indices, schedule, packed, meta_hw, X,
                        ldx, Y, ldy, alpha, ep, true, stream);
+}
+
+int bw_sizes(int dt, int64_t M, int64_t K, const int32_t* keep_blocks_host, size_t* packed_bytes,
+             size_t* indices_count, size_t* workspace_bytes) {
+  if ((dt != SSDNN_F16 && dt != SSDNN_BF16) || M < 0 || K < 0 || M > kMaxDim || K > kMaxDim)
+    return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  if (M > 0 && !keep_blocks_host) return SSDNN_ERR_INVALID_ARG;
+  BwTables tb;
+  const int st = build_bw_tables(M, K, keep_blocks_host, &tb);
+  if (st != SSDNN_OK) return st;
+  if (packed_bytes) *packed_bytes = static_cast<size_t>(128 * 64 * tb.n_blocks * 2);
+  if (indices_count) *indices_count = static_cast<size_t>(tb.n_blocks);
+  if (workspace_bytes) *workspace_bytes = tb.ws_bytes;
+  return SSDNN_OK;
+}
+
+int bw_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, const int32_t* keep_blocks_host,
+                      int32_t* offsets, int32_t* indices, int32_t* schedule, void* packed, void* workspace,
+                      void* stream) {
+  if ((dt != SSDNN_F16 && dt != SSDNN_BF16) || M < 0 || K < 0 || M > kMaxDim || K > kMaxDim)
+    return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  if (M == 0) return SSDNN_OK;
+  if (!keep_blocks_host || !offsets || !schedule) return SSDNN_ERR_INVALID_ARG;
+  BwTables tb;
+  int st = build_bw_tables(M, K, keep_blocks_host, &tb);
+  if (st != SSDNN_OK) return st;
+  if (K > 0 && (!W || ldw < K || !workspace)) return SSDNN_ERR_INVALID_ARG;
+  if (tb.n_blocks > 0 && (!indices || !packed)) return SSDNN_ERR_INVALID_ARG;
+  if ((W && (reinterpret_cast<uintptr_t>(W) & 1u)) || (packed && !aligned16(packed)) ||
+      (workspace && !aligned16(workspace)) || (reinterpret_cast<uintptr_t>(offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(schedule) & 3u) || (indices && (reinterpret_cast<uintptr_t>(indices) & 3u)))
+    return SSDNN_ERR_UNSUPPORTED;
+  auto s = static_cast<cudaStream_t>(stream);
+  auto* ws = static_cast<uint8_t*>(workspace);
+  auto* col_off = reinterpret_cast<int32_t*>(ws + tb.ws_coloff);
+  // Host tables (pageable source: the copy is staged before the call returns).
+  cudaError_t e = cudaMemcpyAsync(offsets, tb.blk_offsets.data(), tb.blk_offsets.size() * sizeof(int32_t),
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(schedule, tb.cols.schedule.data(), tb.cols.schedule.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && K > 0)
+    e = cudaMemcpyAsync(col_off, tb.cols.offsets.data(), tb.cols.offsets.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return SSDNN_ERR_CUDA;
+  if (K == 0) return SSDNN_OK;
+  return from_cuda(launch_bw_prune(dt, W, M, K, ldw, tb.cols.t, offsets, indices, tb.n_blocks, col_off,
+                                   reinterpret_cast<int32_t*>(ws + tb.ws_colidx), schedule, packed,
+                                   reinterpret_cast<float*>(ws + tb.ws_scores),
+                                   reinterpret_cast<float*>(ws + tb.ws_bscores), s));
+}
+
+int bw_gemm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* keep_blocks_host, const int32_t* offsets,
+            const int32_t* indices, const int32_t* schedule, const void* packed, const void* X, int64_t ldx, void* Y,
+            int64_t ldy, void* stream) {
+  return bw_gemm_impl(dt, dt, M, N, K, keep_blocks_host, offsets, indices, schedule, packed, X, ldx, Y, ldy, 1.0f,
+                      nullptr, false, stream);
+}
+
+int bw_gemm_ep(int dt, int out_dt, int64_t M, int64_t N, int64_t K, const int32_t* keep_blocks_host,
+               const int32_t* offsets, const int32_t* indices, const int32_t* schedule, const void* packed,
+               const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+               void* stream) {
+  return bw_gemm_impl(dt, out_dt, M, N, K, keep_blocks_host, offsets, indices, schedule, packed, X, ldx, Y, ldy, alpha,
+                      ep, true, stream);
 }
 
 }  // extern "C"

@@ -72,8 +72,13 @@ struct Params {
   uint32_t* err;
 };
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128, bool PAIR = false>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128, bool PAIR = false,
+          bool BLOCKW = false>
 struct Cfg {
+  // BLOCKW: block-wise sparsity -- per 128-row tile, the packed kept 64-column blocks
+  // of W against the matching 64-row panels of X, each loaded by one TMA box.
+  static constexpr bool BLOCKWISE = BLOCKW;
+  static constexpr bool SCHEDULED = GATHER || BLOCKW;         // work follows the tile schedule
   // PAIR: the two CTAs of a cluster form an SM pair running M = 256 MMAs (each CTA
   // holds 128 rows of A, BN/2 columns of B and its 128 accumulator rows); else
   // CS > 1 CTAs of a cluster share one X panel by multicast.
@@ -137,6 +142,7 @@ struct Cfg {
   static_assert(STAGES >= 2, "the shared-memory ring needs two stages");
   static_assert(B_BOXES * B_BOX_COLS == BN_CTA, "BN must be a multiple of the B box width");
   static_assert(!PAIR || (MT == 1 && CS == 1 && !GATHER), "SM pairs: one 128-row sub-tile per CTA");
+  static_assert(!BLOCKW || (!SPARSE && !GATHER && !PAIR && MT == 1 && CS == 1), "block-wise: dense 128-row tiles");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
   static_assert(MT == 1 || (CS == 1 && !GATHER), "256-row tiles: no cluster, no gather");
   static_assert(CS == 1 || !GATHER, "gathered B rows differ per tile: no multicast");
@@ -288,11 +294,11 @@ __device__ __forceinline__ void stage_packed_row32(uint8_t* buf, uint32_t lane, 
         make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR>
-__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>::THREADS, 1)
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR, bool BLOCKW>
+__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>;
   // Multicast clusters (CS CTAs along M) share each X panel: CTA rank r loads rows
   // [r BK/CS, (r+1) BK/CS) of every B box of a stage and multicasts them to the
   // whole cluster, so a stage is complete only when all CS slices have landed and
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     int issued = 0;
     bool ok = true;
     for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
-      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
+      const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       for (int32_t kb = 0; kb < ui.nk; ++kb) {
         if (*abort_flag) { ok = false; break; }
         if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, p.err);
@@ -395,8 +401,8 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
                                                        (SPARSE ? 2048 * ui.subs : 0));
           // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
           // rows past M read as zeros
-          const int32_t a_col = GATHER ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
-          const int32_t a_row = GATHER ? ui.a_row0 + 128 * kb : ui.m0;
+          const int32_t a_col = C::SCHEDULED ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
+          const int32_t a_row = C::SCHEDULED ? ui.a_row0 + 128 * kb : ui.m0;
           ptx::tma_load_2d(sA, &tmA, &full[stage], a_col, a_row, pol_a);
           if constexpr (SPARSE) {
             for (int mt = 0; mt < ui.subs; ++mt) {
@@ -406,10 +412,12 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
           }
           if constexpr (!GATHER) {
             if constexpr (!C::MCAST) {
+              // block-wise: the X panel of the kb-th kept block of this tile
+              const int32_t krow = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) * C::BK : kb * C::BK;
 #pragma unroll
               for (int bx = 0; bx < C::B_BOXES; ++bx)
-                ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS,
-                                 kb * C::BK, pol_b);
+                ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS, krow,
+                                 pol_b);
             } else {
               const int32_t r0 = static_cast<int32_t>(crank) * C::B_SLICE_ROWS;
 #pragma unroll
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     int meta_slot = 0;
     bool ok = true;
     for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
-      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
+      const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       if (lane == 0) ok = wait_bounded(&acc_empty[acc], acc_phase ^ 1u, p.err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || *abort_flag) { *abort_flag = 1; ok = false; break; }
@@ -572,7 +580,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     const uint16_t* X = static_cast<const uint16_t*>(p.X);
     int32_t idx_ring[kIdxAhead];                     // lane l < 16: X row of stage row 4 l + w
     for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
-      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
+      const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       const int32_t gcol = ui.n0 + col;
       const uint32_t col_bytes = gcol >= p.N ? 0u : static_cast<uint32_t>(min(8, p.N - gcol) * 2);
       auto row_of = [&](int32_t kb) -> int32_t {
@@ -627,7 +635,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
-      const UnitInfo ui = decode_unit<C, GATHER>(p, u, crank);
+      const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       ok = wait_bounded(&acc_full[acc], acc_phase, p.err);
       if (!ok || *abort_flag) { *abort_flag = 1; break; }
       ptx::tc_fence_after();
@@ -759,13 +767,19 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128, bool PAIR = false>
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128, bool PAIR = false,
+          bool BLOCKW = false>
 cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>;
   const int eb = C::EB;
   CUtensorMap tA, tB, tM;
   bool ok;
-  if constexpr (!GATHER) {
+  if constexpr (BLOCKW) {
+    // the packed kept blocks seen as (packed_rows x 64); X as for the dense GEMM
+    ok = make_map(&tA, a.A, eb, 64, a.packed_rows, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::B_SLICE_ROWS,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  } else if constexpr (!GATHER) {
     if constexpr (SPARSE)
       ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, C::BM,
                     CU_TENSOR_MAP_SWIZZLE_64B);
@@ -813,7 +827,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     p.GR = static_cast<int32_t>(ceil_div(p.MG, bands));
   }
   p.nk = static_cast<int32_t>(ceil_div(a.K, C::BK));
-  p.num_units = GATHER ? static_cast<int32_t>(a.nt) * p.NB : p.MG * p.NB;
+  p.num_units = C::SCHEDULED ? static_cast<int32_t>(a.nt) * p.NB : p.MG * p.NB;
   p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : (a.out_dt == SSDNN_E4M3 ? 2 : 0);
   p.act = a.act;
   p.bias = a.bias;
@@ -835,7 +849,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.err = err;
   if (p.num_units == 0) return cudaSuccess;
 
-  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR>;
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   constexpr int CL = C::CLUSTER;
@@ -967,12 +981,15 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
       return sparse ? run_clustered<DT, true, 128>(a, s, err) : run_clustered<DT, false, 128>(a, s, err);
     return sparse ? run_clustered<DT, true, 256>(a, s, err) : run_clustered<DT, false, 256>(a, s, err);
   }
-  // tile-wise: 128-row tiles follow the pattern's tiles
+  // tile-wise and block-wise: 128-row tiles follow the pattern's tiles
   bool narrow = a.N <= 128 || a.nt * ceil_div(a.N, 256) < 2 * sm_count();
   if (const char* e = getenv("SSDNN_GATHER_BN")) narrow = atoi(e) == 128;  // tuning
   if constexpr (DT != 2) {
     if (mode == 2) return narrow ? run<DT, false, true, 128, 1>(a, s, err) : run<DT, false, true, 256, 1>(a, s, err);
     if (mode == 3) return narrow ? run<DT, true, true, 128, 1>(a, s, err) : run<DT, true, true, 256, 1>(a, s, err);
+    if (mode == 4)
+      return narrow ? run<DT, false, false, 128, 1, 1, 128, false, true>(a, s, err)
+                    : run<DT, false, false, 256, 1, 1, 128, false, true>(a, s, err);
   }
   return cudaErrorInvalidValue;
 }

@@ -33,7 +33,8 @@ struct GemmArgs {
   float y_scale = 1.0f;
 };
 
-// mode: 0 dense, 1 sp24, 2 TW (dense packed + gather), 3 TVW (2:4 packed + gather)
+// mode: 0 dense, 1 sp24, 2 TW (dense packed + gather), 3 TVW (2:4 packed + gather),
+// 4 block-wise (dense packed blocks, X panels by TMA)
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err);
 
 // Y = round(y_scale * act(bias[row])) for every element (the fused epilogue of a
@@ -52,6 +53,13 @@ cudaError_t launch_tw_prune(int dt, int tvw, const void* W, int64_t M, int64_t K
                             const TwTables& tabs, const int32_t* offsets, int32_t* indices,
                             const int32_t* schedule, void* packed, uint8_t* meta, uint8_t* meta_hw,
                             float* scores, cudaStream_t s, uint32_t* err);
+
+// Block-wise prune: tile-wise column scores, 64-column block scores, per-tile top-B
+// block selection, the kept blocks' column lists, and the tile-wise dense packing.
+cudaError_t launch_bw_prune(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, const TwTables& tabs,
+                            const int32_t* blk_offsets, int32_t* blk_indices, int64_t n_blocks,
+                            const int32_t* col_offsets, int32_t* col_indices, const int32_t* schedule, void* packed,
+                            float* scores, float* block_scores, cudaStream_t s);
 
 // Tensor-core issue-rate microbenchmark (operands resident on chip), one CTA per SM.
 cudaError_t launch_mma_rate(int dt, int sparse, int n, int iters, cudaStream_t s, uint32_t* err);

@@ -226,7 +226,62 @@ __global__ void __launch_bounds__(512) k_tw_pack(const uint8_t* __restrict__ W, 
   }
 }
 
+// Block-wise: bs[t, b] = fp32 sum over the block's 64 column scores, ascending.
+__global__ void __launch_bounds__(256) k_bw_block_scores(const float* __restrict__ scores, int64_t K, int64_t nt,
+                                                         float* __restrict__ bs) {
+  const int64_t KB = K / 64;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nt * KB) return;
+  const int64_t t = i / KB, b = i - t * KB;
+  const float* src = scores + t * K + 64 * b;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int j = 0; j < 64; ++j) acc = acc + src[j];
+  bs[i] = acc;
+}
+
+// Block-wise: the kept blocks' column lists, in the blocks' order (64 per block).
+__global__ void __launch_bounds__(256) k_bw_expand(const int32_t* __restrict__ blocks, int64_t n_blocks,
+                                                   int32_t* __restrict__ cols) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= 64 * n_blocks) return;
+  cols[i] = 64 * blocks[i >> 6] + static_cast<int32_t>(i & 63);
+}
+
 }  // namespace
+
+cudaError_t launch_bw_prune(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, const TwTables& tabs,
+                            const int32_t* blk_offsets, int32_t* blk_indices, int64_t n_blocks,
+                            const int32_t* col_offsets, int32_t* col_indices, const int32_t* schedule, void* packed,
+                            float* scores, float* block_scores, cudaStream_t s) {
+  if (tabs.nt == 0 || K == 0) return cudaSuccess;
+  const auto* w8 = static_cast<const uint8_t*>(W);
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && ((ldw * 2) % 16 == 0);
+  cudaError_t e;
+  dim3 g(static_cast<unsigned>(ceil_div(ceil_div(K, 8), 256)), static_cast<unsigned>(tabs.nt));
+  if (dt == SSDNN_BF16)
+    k_tw_score<1><<<g, 256, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
+  else
+    k_tw_score<0><<<g, 256, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t nb_all = tabs.nt * (K / 64);
+  k_bw_block_scores<<<static_cast<unsigned>(ceil_div(nb_all, 256)), 256, 0, s>>>(scores, K, tabs.nt, block_scores);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the tile-wise top-L selection, over blocks: (score descending, index ascending)
+  k_tw_select<<<static_cast<unsigned>(tabs.nt), 1024, 0, s>>>(block_scores, K / 64, blk_offsets, blk_indices);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (n_blocks == 0) return cudaSuccess;
+  k_bw_expand<<<static_cast<unsigned>(ceil_div(64 * n_blocks, 256)), 256, 0, s>>>(blk_indices, n_blocks, col_indices);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the kept columns packed exactly as a tile-wise operand
+  dim3 gp(static_cast<unsigned>((tabs.max_R / 64) * 8), static_cast<unsigned>(tabs.nt));
+  auto* pk = static_cast<uint16_t*>(packed);
+  if (dt == SSDNN_BF16)
+    k_tw_pack<1, false><<<gp, 512, 0, s>>>(w8, M, ldw * 2, col_offsets, col_indices, schedule, pk, nullptr, nullptr);
+  else
+    k_tw_pack<0, false><<<gp, 512, 0, s>>>(w8, M, ldw * 2, col_offsets, col_indices, schedule, pk, nullptr, nullptr);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tw_prune(int dt, int tvw, const void* W, int64_t M, int64_t K, int64_t ldw,
                             const TwTables& tabs, const int32_t* offsets, int32_t* indices,

@@ -56,6 +56,11 @@ _SIGS = {
                      _ptr, _i64, C.c_float, _epp, _ptr], C.c_int),
     "sp24_gemm_host": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _i64, _ptr, _i64, C.c_float, _ptr,
                         _ptr, _i64, _ptr, _ptr], C.c_int),
+    "bw_sizes": ([C.c_int, _i64, _i64, _i32p, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
+    "bw_prune_compress": ([C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr], C.c_int),
+    "bw_gemm": ([C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _ptr, _i64, _ptr], C.c_int),
+    "bw_gemm_ep": ([C.c_int, C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _ptr, _i64,
+                    C.c_float, _epp, _ptr], C.c_int),
     "tw_sizes": ([C.c_int, C.c_int, _i64, _i64, _i32p, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz),
                   C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "tw_prune_compress": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
@@ -315,4 +320,63 @@ def tvw_gemm(form: TileWise, X: torch.Tensor, out: torch.Tensor | None = None, o
     else:
         _check(lib.tvw_gemm_ep(form.dt, _DT[out.dtype], int(form.tvw), form.M, N, form.K, *tail, alpha,
                                None if ep is None else C.byref(ep), _stream(X.device)), "tvw_gemm_ep")
+    return out
+
+
+# ---------------------------------------------------------------- block-wise
+@dataclass
+class BlockWise:
+    """A block-wise compressed weight (128 x 64 blocks kept per 128-row tile)."""
+    dt: int
+    M: int
+    K: int
+    keep: np.ndarray          # kept blocks per tile
+    offsets: torch.Tensor     # in blocks
+    indices: torch.Tensor     # kept block indices
+    schedule: torch.Tensor
+    packed: torch.Tensor
+
+
+def bw_sizes(dt: int, M: int, K: int, keep_blocks) -> dict:
+    k = _keep_arr(keep_blocks)
+    out = [_sz() for _ in range(3)]
+    _check(lib.bw_sizes(dt, M, K, _kp(k), *[C.byref(o) for o in out]), "bw_sizes")
+    return dict(zip(("packed_bytes", "indices_count", "workspace_bytes"), (o.value for o in out)))
+
+
+def bw_prune_compress(W: torch.Tensor, keep_blocks, workspace: torch.Tensor | None = None) -> BlockWise:
+    dt = _DT[W.dtype]
+    M, K = W.shape
+    assert W.stride(1) == 1
+    k = _keep_arr(keep_blocks)
+    sz = bw_sizes(dt, M, K, k)
+    dev = W.device
+    nt = (M + 127) // 128
+    offsets = torch.empty(nt + 1, dtype=torch.int32, device=dev)
+    indices = torch.empty(max(1, sz["indices_count"]), dtype=torch.int32, device=dev)
+    schedule = torch.empty(4 * max(1, nt), dtype=torch.int32, device=dev)
+    packed = torch.empty(max(8, sz["packed_bytes"] // 2), dtype=W.dtype, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(16, sz["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    _check(lib.bw_prune_compress(dt, _p(W), M, K, W.stride(0), _kp(k), _p(offsets), _p(indices), _p(schedule),
+                                 _p(packed), _p(workspace), _stream(dev)), "bw_prune_compress")
+    return BlockWise(dt, M, K, k, offsets, indices[:sz["indices_count"]], schedule[:4 * nt],
+                     packed[:sz["packed_bytes"] // 2])
+
+
+def bw_gemm(form: BlockWise, X: torch.Tensor, out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+            alpha: float = 1.0, bias: torch.Tensor | None = None, act: str = "none", y_scale: float = 1.0):
+    """Y = W_bw . X (each tile: its kept blocks against their X panels); with the
+    fused epilogue when bias / act / y_scale / alpha / another output type are given."""
+    N = X.shape[1]
+    if out is None:
+        out = torch.empty((form.M, N), dtype=out_dtype or X.dtype, device=X.device)
+    ep = _epilogue(bias, act, y_scale, form.M)
+    tail = (_kp(form.keep), _p(form.offsets), _p(form.indices), _p(form.schedule), _p(form.packed), _p(X),
+            X.stride(0), _p(out), out.stride(0))
+    if ep is None and out.dtype == X.dtype and alpha == 1.0:
+        _check(lib.bw_gemm(form.dt, form.M, N, form.K, *tail, _stream(X.device)), "bw_gemm")
+    else:
+        _check(lib.bw_gemm_ep(form.dt, _DT[out.dtype], form.M, N, form.K, *tail, alpha,
+                              None if ep is None else C.byref(ep), _stream(X.device)), "bw_gemm_ep")
     return out

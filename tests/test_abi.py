@@ -116,3 +116,16 @@ def test_argument_errors_before_any_device_work(ssdnn):
     # the host-buffer GEMM: block height a multiple of 128, host buffers required
     assert lib.sp24_gemm_host(1, 1, 256, 8, 64, 16, 16, 16, 8, 16, 8, 1.0, 16, 16, 100, None, None) == 1
     assert lib.sp24_gemm_host(1, 1, 256, 8, 64, 16, 16, None, 8, 16, 8, 1.0, 16, 16, 128, None, None) == 1
+    # block-wise: K % 64, kept blocks within range, e4m3 unsupported
+    k = np.array([1, 2], dtype=np.int32)
+    assert lib.bw_sizes(1, 256, 100, k.ctypes.data_as(C.POINTER(C.c_int32)), None, None, None) == 2
+    k3 = np.array([5, 0], dtype=np.int32)
+    assert lib.bw_sizes(1, 256, 256, k3.ctypes.data_as(C.POINTER(C.c_int32)), None, None, None) == 1
+    assert lib.bw_sizes(2, 256, 256, k.ctypes.data_as(C.POINTER(C.c_int32)), None, None, None) == 2
+
+
+def test_bw_sizes_match_layout(ssdnn):
+    s = ssdnn.bw_sizes(ssdnn.BF16, 300, 256, np.array([1, 4, 0], dtype=np.int32))
+    assert s["packed_bytes"] == 128 * 64 * 5 * 2
+    assert s["indices_count"] == 5
+    assert s["workspace_bytes"] >= 3 * 256 * 4 + 3 * 4 * 4 + 4 * 4 + 64 * 5 * 4
