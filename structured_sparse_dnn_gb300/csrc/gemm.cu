@@ -310,8 +310,18 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
   constexpr int CL = C::CLUSTER;
   const uint32_t crank = (CL > 1) ? ptx::cluster_ctarank() : 0u;
   const bool leader = !PAIR || (crank & 1u) == 0u;
-  const int32_t unit0 = static_cast<int32_t>(blockIdx.x) / CL;
-  const int32_t unit_stride = static_cast<int32_t>(gridDim.x) / CL;
+  // Work units are dealt in rounds of one unit per cluster, alternating direction
+  // (round r gives unit r S + c to cluster c for even r, r S + S - 1 - c for odd
+  // r): with tiles ordered by kept count descending, a cluster that took a long
+  // unit in one round takes a short one in the next.
+  const int32_t unit_c = static_cast<int32_t>(blockIdx.x) / CL;
+  const int32_t unit_S = static_cast<int32_t>(gridDim.x) / CL;
+  auto unit_at = [&](int32_t r) -> int32_t {
+    const int32_t base = r * unit_S;
+    if (base >= p.num_units) return -1;
+    const int32_t u = base + ((r & 1) ? unit_S - 1 - unit_c : unit_c);
+    return u < p.num_units ? u : -1;
+  };
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1u);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -372,7 +382,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     uint32_t phase = 0;
     int issued = 0;
     bool ok = true;
-    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+    for (int32_t r = 0, u = unit_at(0); u >= 0 && ok; u = unit_at(++r)) {
       const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       for (int32_t kb = 0; kb < ui.nk; ++kb) {
         if (*abort_flag) { ok = false; break; }
@@ -463,7 +473,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     uint32_t acc_phase = 0;
     int meta_slot = 0;
     bool ok = true;
-    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+    for (int32_t r = 0, u = unit_at(0); u >= 0 && ok; u = unit_at(++r)) {
       const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       if (lane == 0) ok = wait_bounded(&acc_empty[acc], acc_phase ^ 1u, p.err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -579,7 +589,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     bool ok = true;
     const uint16_t* X = static_cast<const uint16_t*>(p.X);
     int32_t idx_ring[kIdxAhead];                     // lane l < 16: X row of stage row 4 l + w
-    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+    for (int32_t r = 0, u = unit_at(0); u >= 0 && ok; u = unit_at(++r)) {
       const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       const int32_t gcol = ui.n0 + col;
       const uint32_t col_bytes = gcol >= p.N ? 0u : static_cast<uint32_t>(min(8, p.N - gcol) * 2);
@@ -634,7 +644,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int32_t u = unit0; u < p.num_units && ok; u += unit_stride) {
+    for (int32_t r = 0, u = unit_at(0); u >= 0 && ok; u = unit_at(++r)) {
       const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       ok = wait_bounded(&acc_full[acc], acc_phase, p.err);
       if (!ok || *abort_flag) { *abort_flag = 1; break; }
