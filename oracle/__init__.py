@@ -16,6 +16,8 @@ What it computes, each function citing the page passage it follows:
                    output scaling and rounding (e4m3 output included).
   * bw          -- block-wise sparsity (128 x 64 blocks of a tile row kept by
                    block score), packing and the block-sparse GEMM.
+  * ew          -- element-wise (unstructured) magnitude pruning to CSR and the
+                   sparse x dense product.
   * tw          -- tile-wise scores, per-tile top-L selection, packing of the
                    kept columns, the tile-vector-wise hybrid, the tile schedule.
 
@@ -27,4 +29,4 @@ the CUDA path decides it in fp32 in that order.
 Every function has a pin in tests/ other than itself (closed forms, brute force
 on tiny inputs, invariants, hand-derived fixtures in tests/golden/).
 """
-from . import codecs, sp24, gemm, tw, epilogue, bw  # noqa: F401
+from . import codecs, sp24, gemm, tw, epilogue, bw, ew  # noqa: F401
