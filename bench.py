@@ -440,6 +440,21 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
     form_bw = ss.bw_prune_compress(Wt, keep_b, work_b)
     t_bw = statistics.mean(timed_steps(lambda: ss.bw_gemm(form_bw, Xt, out=Yt), steps, 2, flush, stream))
     flops_bw = 2.0 * 128 * 64 * float(keep_b.sum()) * tw.N
+    # element-wise / unstructured (NEXT-3): CSR x dense on the CUDA cores at 90 % and 95 % sparsity
+    ew_rows = {}
+    szw = ss.ew_sizes(ss.BF16, tw.M, tw.K, tw.K)
+    work_e = torch.empty(szw["workspace_bytes"], dtype=torch.uint8, device=dev)
+    for sparsity in (0.90, 0.95):
+        k_e = round((1.0 - sparsity) * tw.K)
+        t_ep = statistics.mean(timed_steps(lambda: ss.ew_prune_compress(Wt, k_e, work_e), 3, 1, flush, stream))
+        form_e = ss.ew_prune_compress(Wt, k_e, work_e)
+        t_e = statistics.mean(timed_steps(lambda: ss.ew_spmm(form_e, Xt, out=Yt), 5, 2, flush, stream))
+        ew_rows[f"{int(sparsity * 100)}%"] = {
+            "prune_ms": round(t_ep, 4), "spmm_ms": round(t_e, 4),
+            "effective_TFLOP/s": round(2.0 * tw.M * k_e * tw.N / (t_e * 1e-3) / 1e12, 1),
+            "speedup_over_dense": round(t_dense / t_e, 3)}
+        del form_e
+    del work_e
     dens = 128.0 * keep.sum() / (tw.M * tw.K)
     flops_tw = 2.0 * 128 * float(keep.sum()) * tw.N
     flops_tvw = 2.0 * 128 * float(keep4.sum()) * tw.N * 0.5
@@ -455,6 +470,7 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
         "bw_effective_TFLOP/s": round(flops_bw / (t_bw * 1e-3) / 1e12, 1),
         "bw_kept_fraction": round(float(keep_b.sum()) * 64 / tw.K / len(keep_b), 4),
         "bw_speedup_over_dense": round(t_dense / t_bw, 3),
+        "ew_unstructured": ew_rows,
         "sparsity": round(1 - float(dens), 4),
     }
     return rows

@@ -217,6 +217,26 @@ int bw_gemm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* keep_blocks_
             const int32_t* indices, const int32_t* schedule, const void* packed, const void* X, int64_t ldx, void* Y,
             int64_t ldy, void* stream);
 
+/* ---------------------------------------------------------- element-wise ----
+ * Unstructured sparsity ("SparseRT: Accelerating Unstructured Sparsity on GPUs
+ * for Deep Learning Inference", Abstract: individually pruned weights, 90-95 %
+ * sparsity, fully connected / 1x1 layers as sparse x dense products; the EW
+ * pattern of the tiled-GEMM page, Figure 5 caption). Readings: every row keeps
+ * the same count k of its largest |w| (stored bits with the sign cleared, ties to
+ * the lower column), listed in ascending column order, as CSR:
+ *   row_ptr  M + 1 int32 (row_ptr[i] = i k), col_idx M k int32, vals M k values
+ *            (stored bits copied).
+ * ew_prune_compress needs ew_sizes' workspace (M x K fp32 magnitudes). ew_spmm
+ * takes any CSR (row_ptr non-decreasing, columns ascending within a row, all
+ * < K): Y = W_ew . X, fp32 accumulation on the CUDA cores, one RNE conversion to
+ * dt. fp16/bf16 only (E4M3: SSDNN_ERR_UNSUPPORTED). */
+int ew_sizes(int dt, int64_t M, int64_t K, int64_t k, size_t* vals_bytes, size_t* indices_count,
+             size_t* workspace_bytes);
+int ew_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, int64_t k, int32_t* row_ptr,
+                      int32_t* col_idx, void* vals, void* workspace, void* stream);
+int ew_spmm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx,
+            const void* vals, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream);
+
 /* --------------------------------------------------- fused layer epilogue ----
  * A pruned fully connected layer or 1x1 convolution runs as one of the GEMMs
  * above ("Accelerating Sparse DNNs Based on Tiled GEMM", Abstract), and the step

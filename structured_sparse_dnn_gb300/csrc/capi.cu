@@ -604,4 +604,43 @@ int bw_gemm_ep(int dt, int out_dt, int64_t M, int64_t N, int64_t K, const int32_
                       ep, true, stream);
 }
 
+int ew_sizes(int dt, int64_t M, int64_t K, int64_t k, size_t* vals_bytes, size_t* indices_count,
+             size_t* workspace_bytes) {
+  if ((dt != SSDNN_F16 && dt != SSDNN_BF16) || M < 0 || K < 0 || k < 0 || M > kMaxDim || K > kMaxDim || k > K)
+    return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  if (M * k > kMaxDim) return SSDNN_ERR_UNSUPPORTED;
+  if (vals_bytes) *vals_bytes = static_cast<size_t>(M * k * 2);
+  if (indices_count) *indices_count = static_cast<size_t>(M * k);
+  if (workspace_bytes) *workspace_bytes = static_cast<size_t>(M * K * 4);
+  return SSDNN_OK;
+}
+
+int ew_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, int64_t k, int32_t* row_ptr,
+                      int32_t* col_idx, void* vals, void* workspace, void* stream) {
+  int st = ew_sizes(dt, M, K, k, nullptr, nullptr, nullptr);
+  if (st != SSDNN_OK) return st;
+  if (!row_ptr) return SSDNN_ERR_INVALID_ARG;
+  if (M > 0 && k > 0 && (!W || ldw < K || !col_idx || !vals || !workspace)) return SSDNN_ERR_INVALID_ARG;
+  if ((W && (reinterpret_cast<uintptr_t>(W) & 1u)) || (vals && (reinterpret_cast<uintptr_t>(vals) & 1u)) ||
+      (workspace && !aligned16(workspace)) || (reinterpret_cast<uintptr_t>(row_ptr) & 3u) ||
+      (col_idx && (reinterpret_cast<uintptr_t>(col_idx) & 3u)))
+    return SSDNN_ERR_UNSUPPORTED;
+  return from_cuda(launch_ew_prune(dt, W, M, K, ldw, k, row_ptr, col_idx, vals, static_cast<float*>(workspace),
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int ew_spmm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx,
+            const void* vals, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream) {
+  if (dt != SSDNN_F16 && dt != SSDNN_BF16) return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  const int st = check_gemm_io(dt, false, M, N, K, X, ldx, 2, Y, ldy);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (!row_ptr || (K > 0 && (!col_idx || !vals))) return SSDNN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(row_ptr) & 3u) || (col_idx && (reinterpret_cast<uintptr_t>(col_idx) & 3u)) ||
+      (vals && (reinterpret_cast<uintptr_t>(vals) & 1u)))
+    return SSDNN_ERR_UNSUPPORTED;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(Y, ldy, M, N, 2, s);
+  return from_cuda(launch_ew_spmm(dt, M, N, K, row_ptr, col_idx, vals, X, ldx, Y, ldy, s));
+}
+
 }  // extern "C"

@@ -61,6 +61,12 @@ cudaError_t launch_bw_prune(int dt, const void* W, int64_t M, int64_t K, int64_t
                             const int32_t* col_offsets, int32_t* col_indices, const int32_t* schedule, void* packed,
                             float* scores, float* block_scores, cudaStream_t s);
 
+// Element-wise (unstructured) prune to CSR (k kept per row) and the CSR x dense product.
+cudaError_t launch_ew_prune(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, int64_t k, int32_t* row_ptr,
+                            int32_t* col_idx, void* vals, float* mag, cudaStream_t s);
+cudaError_t launch_ew_spmm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx,
+                           const void* vals, const void* X, int64_t ldx, void* Y, int64_t ldy, cudaStream_t s);
+
 // Tensor-core issue-rate microbenchmark (operands resident on chip), one CTA per SM.
 cudaError_t launch_mma_rate(int dt, int sparse, int n, int iters, cudaStream_t s, uint32_t* err);
 

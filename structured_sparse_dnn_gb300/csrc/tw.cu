@@ -283,6 +283,13 @@ cudaError_t launch_bw_prune(int dt, const void* W, int64_t M, int64_t K, int64_t
   return cudaGetLastError();
 }
 
+cudaError_t launch_row_select(const float* scores, int64_t rows, int64_t K, const int32_t* offsets, int32_t* indices,
+                              cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  k_tw_select<<<static_cast<unsigned>(rows), 1024, 0, s>>>(scores, K, offsets, indices);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_tw_prune(int dt, int tvw, const void* W, int64_t M, int64_t K, int64_t ldw,
                             const TwTables& tabs, const int32_t* offsets, int32_t* indices,
                             const int32_t* schedule, void* packed, uint8_t* meta, uint8_t* meta_hw,

@@ -61,6 +61,9 @@ _SIGS = {
     "bw_gemm": ([C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _ptr, _i64, _ptr], C.c_int),
     "bw_gemm_ep": ([C.c_int, C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _ptr, _i64,
                     C.c_float, _epp, _ptr], C.c_int),
+    "ew_sizes": ([C.c_int, _i64, _i64, _i64, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
+    "ew_prune_compress": ([C.c_int, _ptr, _i64, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], C.c_int),
+    "ew_spmm": ([C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, _i64, _ptr, _i64, _ptr], C.c_int),
     "tw_sizes": ([C.c_int, C.c_int, _i64, _i64, _i32p, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz),
                   C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "tw_prune_compress": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
@@ -379,4 +382,54 @@ def bw_gemm(form: BlockWise, X: torch.Tensor, out: torch.Tensor | None = None, o
     else:
         _check(lib.bw_gemm_ep(form.dt, _DT[out.dtype], form.M, N, form.K, *tail, alpha,
                               None if ep is None else C.byref(ep), _stream(X.device)), "bw_gemm_ep")
+    return out
+
+
+# ---------------------------------------------------------------- element-wise
+@dataclass
+class ElementWise:
+    """An element-wise (unstructured) sparse weight in CSR form (k kept per row)."""
+    dt: int
+    M: int
+    K: int
+    k: int
+    row_ptr: torch.Tensor
+    col_idx: torch.Tensor
+    vals: torch.Tensor
+    col_buf: torch.Tensor | None = None   # the allocations behind col_idx / vals (at least one element,
+    val_buf: torch.Tensor | None = None   # so that an empty CSR still passes valid pointers)
+
+
+def ew_sizes(dt: int, M: int, K: int, k: int) -> dict:
+    out = [_sz() for _ in range(3)]
+    _check(lib.ew_sizes(dt, M, K, k, *[C.byref(o) for o in out]), "ew_sizes")
+    return dict(zip(("vals_bytes", "indices_count", "workspace_bytes"), (o.value for o in out)))
+
+
+def ew_prune_compress(W: torch.Tensor, k: int, workspace: torch.Tensor | None = None) -> ElementWise:
+    dt = _DT[W.dtype]
+    M, K = W.shape
+    assert W.stride(1) == 1
+    sz = ew_sizes(dt, M, K, k)
+    dev = W.device
+    row_ptr = torch.empty(M + 1, dtype=torch.int32, device=dev)
+    col_idx = torch.empty(max(1, sz["indices_count"]), dtype=torch.int32, device=dev)
+    vals = torch.empty(max(1, sz["indices_count"]), dtype=W.dtype, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(16, sz["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    _check(lib.ew_prune_compress(dt, _p(W), M, K, W.stride(0), k, _p(row_ptr), _p(col_idx), _p(vals), _p(workspace),
+                                 _stream(dev)), "ew_prune_compress")
+    n = sz["indices_count"]
+    return ElementWise(dt, M, K, k, row_ptr, col_idx[:n], vals[:n], col_idx, vals)
+
+
+def ew_spmm(form: ElementWise, X: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y = W_ew . X on the CUDA cores (fp32 accumulation, one rounding to X's type)."""
+    N = X.shape[1]
+    if out is None:
+        out = torch.empty((form.M, N), dtype=X.dtype, device=X.device)
+    cols = form.col_buf if form.col_buf is not None else form.col_idx
+    vals = form.val_buf if form.val_buf is not None else form.vals
+    _check(lib.ew_spmm(form.dt, form.M, N, form.K, _p(form.row_ptr), _p(cols), _p(vals), _p(X),
+                       X.stride(0), _p(out), out.stride(0), _stream(X.device)), "ew_spmm")
     return out

@@ -129,3 +129,6 @@ def test_bw_sizes_match_layout(ssdnn):
     assert s["packed_bytes"] == 128 * 64 * 5 * 2
     assert s["indices_count"] == 5
     assert s["workspace_bytes"] >= 3 * 256 * 4 + 3 * 4 * 4 + 4 * 4 + 64 * 5 * 4
+    # element-wise: k > K invalid, e4m3 unsupported
+    assert ssdnn.lib.ew_sizes(1, 8, 16, 17, None, None, None) == 1
+    assert ssdnn.lib.ew_sizes(2, 8, 16, 4, None, None, None) == 2
