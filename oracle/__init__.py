@@ -18,6 +18,8 @@ What it computes, each function citing the page passage it follows:
                    block score), packing and the block-sparse GEMM.
   * ew          -- element-wise (unstructured) magnitude pruning to CSR and the
                    sparse x dense product.
+  * conv        -- 3x3 convolution (stride 1, padding 1) of NHWC activations with a
+                   2:4-sparse or dense filter, through the im2col matrix.
   * tw          -- tile-wise scores, per-tile top-L selection, packing of the
                    kept columns, the tile-vector-wise hybrid, the tile schedule.
 
@@ -29,4 +31,4 @@ the CUDA path decides it in fp32 in that order.
 Every function has a pin in tests/ other than itself (closed forms, brute force
 on tiny inputs, invariants, hand-derived fixtures in tests/golden/).
 """
-from . import codecs, sp24, gemm, tw, epilogue, bw, ew  # noqa: F401
+from . import codecs, sp24, gemm, tw, epilogue, bw, ew, conv  # noqa: F401
