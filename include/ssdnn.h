@@ -237,6 +237,24 @@ int ew_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, 
 int ew_spmm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx,
             const void* vals, const void* X, int64_t ldx, void* Y, int64_t ldy, void* stream);
 
+/* ------------------------------------------------------ 3x3 convolution ----
+ * Sparse 3x3 convolutions (ResNet-50 use cases: "SparseRT: Accelerating
+ * Unstructured Sparsity on GPUs for Deep Learning Inference", Abstract) with a
+ * 2:4 filter ("Accelerating Sparse Deep Neural Networks", Abstract), run as an
+ * implicit GEMM on the (sparse) tensor cores. Stride 1, zero padding 1.
+ * Readings: X is NHWC (Nb, H, W, Cin), 16-byte aligned; the filter is
+ * (Cout, 3, 3, Cin) flattened to Cout x 9 Cin with column (r 3 + s) Cin + c, so its
+ * 2:4 form is sp24_prune_compress of that matrix (K = 9 Cin); Y is Cout x (Nb H W),
+ * Y[co, (n H + h) W + w] = alpha sum_{r,s,c} W[co, r, s, c] X[n, h + r - 1, w + s - 1, c]
+ * (zero outside the image), pitch ldy >= Nb H W, fp32 accumulation, one RNE
+ * conversion to out_dt (fp16 / bf16). Cin % 64 == 0 and W <= 224, else
+ * SSDNN_ERR_UNSUPPORTED; 16-bit data only. */
+int sp24_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W, const void* values,
+                 const uint8_t* meta_hw, const void* X, void* Y, int64_t ldy, float alpha, void* stream);
+/* The same with a dense filter Wf (Cout x 9 Cin, pitch ldw): the same-family baseline. */
+int dense_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W, const void* Wf,
+                  int64_t ldw, const void* X, void* Y, int64_t ldy, float alpha, void* stream);
+
 /* --------------------------------------------------- fused layer epilogue ----
  * A pruned fully connected layer or 1x1 convolution runs as one of the GEMMs
  * above ("Accelerating Sparse DNNs Based on Tiled GEMM", Abstract), and the step

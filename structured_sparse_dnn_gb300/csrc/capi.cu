@@ -643,4 +643,52 @@ int ew_spmm(int dt, int64_t M, int64_t N, int64_t K, const int32_t* row_ptr, con
   return from_cuda(launch_ew_spmm(dt, M, N, K, row_ptr, col_idx, vals, X, ldx, Y, ldy, s));
 }
 
+// 3x3 convolution (implicit GEMM), shared checks: 16-bit data, C_in a multiple of 64,
+// image width at most 224, output C_out x (N H W) with a 16-byte-aligned pitch.
+static int conv_impl(int sparse, int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W,
+                     const void* A, int64_t lda, const uint8_t* meta_hw, const void* X, void* Y, int64_t ldy,
+                     float alpha, void* stream) {
+  if (dt != SSDNN_F16 && dt != SSDNN_BF16) return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  if (Cout < 0 || Cin < 0 || Nb < 0 || H < 0 || W < 0) return SSDNN_ERR_INVALID_ARG;
+  if (Cout > kMaxDim || Nb * H * W > kMaxDim || 9 * Cin > kMaxDim || H > kMaxDim) return SSDNN_ERR_INVALID_ARG;
+  if (Cin % 64 || W > 224) return SSDNN_ERR_UNSUPPORTED;
+  const int64_t M = Cout, N = Nb * H * W, K = 9 * Cin;
+  // X is NHWC, not an N-pitch matrix: only its base alignment applies (passed as a pitch that checks clean)
+  int st = check_gemm_io(out_dt, false, M, N, K, X, round_up(N, 8), 2, Y, ldy);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(Y, ldy, M, N, 2, s);
+  if (!A || (sparse && !meta_hw) || (!sparse && lda < K)) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(A) || (sparse && !aligned16(meta_hw)) || (!sparse && (lda * 2) % 16)) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = A;
+  a.lda = sparse ? K / 2 : lda;
+  a.meta_hw = meta_hw;
+  a.X = X;
+  a.ldx = N;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  a.conv_cin = Cin;
+  a.conv_h = H;
+  a.conv_w = W;
+  a.conv_nb = Nb;
+  return from_cuda(launch_gemm(sparse ? 5 : 6, a, s, error_word()));
+}
+
+int sp24_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W, const void* values,
+                 const uint8_t* meta_hw, const void* X, void* Y, int64_t ldy, float alpha, void* stream) {
+  return conv_impl(1, dt, out_dt, Cout, Cin, Nb, H, W, values, 0, meta_hw, X, Y, ldy, alpha, stream);
+}
+
+int dense_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W, const void* Wf,
+                  int64_t ldw, const void* X, void* Y, int64_t ldy, float alpha, void* stream) {
+  return conv_impl(0, dt, out_dt, Cout, Cin, Nb, H, W, Wf, ldw, nullptr, X, Y, ldy, alpha, stream);
+}
+
 }  // extern "C"

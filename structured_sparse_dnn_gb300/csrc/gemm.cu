@@ -70,11 +70,19 @@ struct Params {
   uint8_t* Y;
   int64_t ldy;              // elements
   uint32_t* err;
+  // 3x3 convolution: image geometry and the pixel patch of one work unit
+  int32_t conv_cin, conv_h, conv_w, conv_rows;  // C_in, H, W, image rows per patch
+  int32_t conv_patches;                         // patches per image
+  uint32_t conv_box_bytes;                      // bytes one activation box delivers
 };
 
 template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128, bool PAIR = false,
-          bool BLOCKW = false>
+          bool BLOCKW = false, bool CONV = false>
 struct Cfg {
+  // CONV: 3x3 convolution as an implicit GEMM -- the B operand of a K stage is one
+  // tap (r, s) and 64 input channels of a patch of image rows, loaded K-major by one
+  // 4-D TMA box of the NHWC activations (the zero padding is the box's out-of-range fill).
+  static constexpr bool CONVOLUTION = CONV;
   // BLOCKW: block-wise sparsity -- per 128-row tile, the packed kept 64-column blocks
   // of W against the matching 64-row panels of X, each loaded by one TMA box.
   static constexpr bool BLOCKWISE = BLOCKW;
@@ -114,7 +122,7 @@ struct Cfg {
   // Output staging (all but TW/TVW): each epilogue warp converts a 32 x 32 chunk
   // into one of two 2 KB shared-memory buffers and a TMA store writes it out, so
   // the accumulator is drained without waiting on global stores.
-  static constexpr bool STAGED = !GATHER;
+  static constexpr bool STAGED = !GATHER && !CONV;
   static constexpr int STAGING_BYTES = STAGED ? EPI_WARPS * 4096 : 0;
   static constexpr int STAGES_RAW = (220 * 1024 - STAGING_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -137,12 +145,15 @@ struct Cfg {
   static constexpr int META_COL0 = NACC * ACC_COLS;         // TMEM columns after the accumulators
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC = ptx::idesc(Elem<DT>::mma_fmt, Elem<DT>::mma_fmt, SPARSE, PAIR ? 256 : 128,
-                                               BN, false, true);
+                                               BN, false, !CONV);
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(STAGES >= 2, "the shared-memory ring needs two stages");
-  static_assert(B_BOXES * B_BOX_COLS == BN_CTA, "BN must be a multiple of the B box width");
+  static_assert(CONV || B_BOXES * B_BOX_COLS == BN_CTA, "BN must be a multiple of the B box width");
+  static_assert(BN % 32 == 0, "the epilogue drains 32-column chunks");
   static_assert(!PAIR || (MT == 1 && CS == 1 && !GATHER), "SM pairs: one 128-row sub-tile per CTA");
   static_assert(!BLOCKW || (!SPARSE && !GATHER && !PAIR && MT == 1 && CS == 1), "block-wise: dense 128-row tiles");
+  static_assert(!CONV || (!GATHER && !PAIR && !BLOCKW && MT == 1 && CS == 1 && Elem<DT>::bytes == 2),
+                "convolution: 16-bit, 128-row tiles");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
   static_assert(MT == 1 || (CS == 1 && !GATHER), "256-row tiles: no cluster, no gather");
   static_assert(CS == 1 || !GATHER, "gathered B rows differ per tile: no multicast");
@@ -164,11 +175,33 @@ struct UnitInfo {
   int32_t meta_blk0;  // first metadata block index
   int32_t idx_base;   // offsets[t] (TW/TVW)
   int32_t L;          // kept count (TW/TVW)
+  int32_t ncols;      // valid output columns from n0 (convolution patches)
+  int32_t img, h0;    // convolution: image and first image row of the patch
 };
 
 template <typename C, bool GATHER>
 __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint32_t crank) {
   UnitInfo ui;
+  ui.ncols = 0;
+  ui.img = 0;
+  ui.h0 = 0;
+  if constexpr (C::CONVOLUTION) {
+    // units: 128-row blocks of C_out fastest, then pixel patches (image, row block)
+    const int32_t mb = u % p.MB, patch = u / p.MB;
+    ui.img = patch / p.conv_patches;
+    ui.h0 = (patch - ui.img * p.conv_patches) * p.conv_rows;
+    ui.phantom = false;
+    ui.m0 = mb * 128;
+    ui.n0 = (ui.img * p.conv_h + ui.h0) * p.conv_w;
+    ui.ncols = min(p.conv_rows, p.conv_h - ui.h0) * p.conv_w;
+    ui.nk = p.nk;
+    ui.a_row0 = ui.m0;
+    ui.meta_blk0 = mb * p.nk;
+    ui.subs = 1;
+    ui.idx_base = 0;
+    ui.L = 0;
+    return ui;
+  }
   if constexpr (!GATHER) {
     // Bands of GR M groups: inside a band the M index runs fastest, then N, so the
     // CTAs in flight share a few weight rows and a few X panels and both stay in
@@ -251,7 +284,7 @@ __device__ __forceinline__ void store_packed_row32(uint8_t* dst_row, int32_t n0,
                                                    const uint32_t (&w)[16], uint64_t pol) {
   if (out_dt == 2) {
     uint8_t* dst = dst_row + n0;
-    if (n0 + 32 <= N) {
+    if (n0 + 32 <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
       ptx::st_global_v4_hint(dst, w[0], w[1], w[2], w[3], pol);
       ptx::st_global_v4_hint(dst + 16, w[4], w[5], w[6], w[7], pol);
     } else {
@@ -262,7 +295,7 @@ __device__ __forceinline__ void store_packed_row32(uint8_t* dst_row, int32_t n0,
     return;
   }
   uint16_t* dst = reinterpret_cast<uint16_t*>(dst_row) + n0;
-  if (n0 + 32 <= N) {
+  if (n0 + 32 <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
 #pragma unroll
     for (int v = 0; v < 4; ++v)
       ptx::st_global_v4_hint(reinterpret_cast<uint4*>(dst) + v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3],
@@ -294,11 +327,11 @@ __device__ __forceinline__ void stage_packed_row32(uint8_t* buf, uint32_t lane, 
         make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR, bool BLOCKW>
-__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>::THREADS, 1)
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR, bool BLOCKW, bool CONV>
+__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>;
   // Multicast clusters (CS CTAs along M) share each X panel: CTA rank r loads rows
   // [r BK/CS, (r+1) BK/CS) of every B box of a stage and multicasts them to the
   // whole cluster, so a stage is complete only when all CS slices have landed and
@@ -407,7 +440,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
               ptx::tma_load_2d_pair(sB + bx * C::B_BOX_BYTES, &tmB, bar, n_half + bx * C::B_BOX_COLS, kb * C::BK,
                                     pol_b);
           } else {
-          ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0 : C::B_BYTES) +
+          ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0u : (CONV ? p.conv_box_bytes : C::B_BYTES)) +
                                                        (SPARSE ? 2048 * ui.subs : 0));
           // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
           // rows past M read as zeros
@@ -420,7 +453,14 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
               ptx::bulk_load(sM + mt * 2048, src, 2048, &full[stage], pol_a);
             }
           }
-          if constexpr (!GATHER) {
+          if constexpr (CONV) {
+            // tap (r, s) and 64 input channels of K stage kb, for the patch's image rows
+            // shifted by the tap (out-of-range rows and columns read as zeros)
+            const int32_t cblocks = p.conv_cin / 64;
+            const int32_t tap = kb / cblocks, c0 = (kb - tap * cblocks) * 64;
+            const int32_t r = tap / 3, sx = tap - 3 * r;
+            ptx::tma_load_4d(sB, &tmB, &full[stage], c0, sx - 1, ui.h0 + r - 1, ui.img, pol_b);
+          } else if constexpr (!GATHER) {
             if constexpr (!C::MCAST) {
               // block-wise: the X panel of the kb-th kept block of this tile
               const int32_t krow = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) * C::BK : kb * C::BK;
@@ -507,7 +547,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
-            const uint64_t bdesc = ptx::sdesc(sB + j * C::MMA_K * C::B_ROW, C::B_BOX_BYTES, C::B_SBO, C::B_SWZ);
+            // B: MN-major boxes, or (convolution) K-major pixel rows of 128 bytes
+            const uint64_t bdesc = CONV ? ptx::sdesc(sB + j * C::MMA_K * C::EB, 16, 1024, 2)
+                                        : ptx::sdesc(sB + j * C::MMA_K * C::B_ROW, C::B_BOX_BYTES, C::B_SBO, C::B_SWZ);
             const uint32_t d_sub = d_tmem + static_cast<uint32_t>(mt * BN);
             const uint32_t a_sub = sA + static_cast<uint32_t>(mt * C::A_SUB_BYTES);
             if constexpr (SPARSE) {
@@ -710,8 +752,10 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
             ptx::bulk_commit();
           }
         } else {
-          if (!row_ok || n0 >= p.N) continue;
-          store_packed_row32(yrow, n0, p.N, p.out_dt, w, pol_y);
+          // convolution patches end at their last valid image row
+          const int32_t n_lim = CONV ? ui.n0 + ui.ncols : p.N;
+          if (!row_ok || n0 >= n_lim) continue;
+          store_packed_row32(yrow, n0, n_lim, p.out_dt, w, pol_y);
         }
       }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
@@ -770,6 +814,22 @@ bool make_map(CUtensorMap* m, const void* base, int eb, uint64_t cols, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+// 4-D tensor map over NHWC activations seen innermost-first as (C, W, H, N),
+// one box = 64 channels x box_w columns x box_h rows x 1 image, 128B swizzle.
+bool make_map_nhwc(CUtensorMap* m, const void* base, uint64_t C_, uint64_t W_, uint64_t H_, uint64_t N_,
+                   uint32_t box_w, uint32_t box_h) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {C_, W_, H_, N_};
+  const cuuint64_t strides[3] = {C_ * 2, W_ * C_ * 2, H_ * W_ * C_ * 2};
+  const cuuint32_t box[4] = {64, box_w, box_h, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -778,13 +838,26 @@ int sm_count() {
 }
 
 template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128, bool PAIR = false,
-          bool BLOCKW = false>
+          bool BLOCKW = false, bool CONV = false>
 cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>;
   const int eb = C::EB;
   CUtensorMap tA, tB, tM;
   bool ok;
-  if constexpr (BLOCKW) {
+  int32_t conv_rows = 0;
+  if constexpr (CONV) {
+    // A as for the 2:4 / dense GEMM over the flattened filter; X as NHWC boxes of
+    // BN / W whole image rows
+    conv_rows = static_cast<int32_t>(BN / a.conv_w);
+    if constexpr (SPARSE)
+      ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, C::BM,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+    else
+      ok = make_map(&tA, a.A, eb, a.K, a.M, a.lda * eb, 128 / eb, C::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && conv_rows >= 1 &&
+         make_map_nhwc(&tB, a.X, a.conv_cin, a.conv_w, a.conv_h, a.conv_nb, static_cast<uint32_t>(a.conv_w),
+                       static_cast<uint32_t>(conv_rows));
+  } else if constexpr (BLOCKW) {
     // the packed kept blocks seen as (packed_rows x 64); X as for the dense GEMM
     ok = make_map(&tA, a.A, eb, 64, a.packed_rows, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::B_SLICE_ROWS,
@@ -838,6 +911,15 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   }
   p.nk = static_cast<int32_t>(ceil_div(a.K, C::BK));
   p.num_units = C::SCHEDULED ? static_cast<int32_t>(a.nt) * p.NB : p.MG * p.NB;
+  if constexpr (CONV) {
+    p.conv_cin = static_cast<int32_t>(a.conv_cin);
+    p.conv_h = static_cast<int32_t>(a.conv_h);
+    p.conv_w = static_cast<int32_t>(a.conv_w);
+    p.conv_rows = conv_rows;
+    p.conv_patches = static_cast<int32_t>(ceil_div(a.conv_h, conv_rows));
+    p.conv_box_bytes = static_cast<uint32_t>(128 * conv_rows * a.conv_w);
+    p.num_units = p.MB * static_cast<int32_t>(a.conv_nb) * p.conv_patches;
+  }
   p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : (a.out_dt == SSDNN_E4M3 ? 2 : 0);
   p.act = a.act;
   p.bias = a.bias;
@@ -859,7 +941,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.err = err;
   if (p.num_units == 0) return cudaSuccess;
 
-  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW>;
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   constexpr int CL = C::CLUSTER;
@@ -990,6 +1072,20 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
     if (c.bn == 128)
       return sparse ? run_clustered<DT, true, 128>(a, s, err) : run_clustered<DT, false, 128>(a, s, err);
     return sparse ? run_clustered<DT, true, 256>(a, s, err) : run_clustered<DT, false, 256>(a, s, err);
+  }
+  if (mode == 5 || mode == 6) {
+    // 3x3 convolution: N tiles of whole image rows, 224 columns (128 when that leaves
+    // fewer than two tiles per SM)
+    if constexpr (EB == 2) {
+      const int64_t units224 = ceil_div(a.M, 128) * a.conv_nb * ceil_div(a.conv_h, 224 / a.conv_w);
+      const bool narrow_c = a.conv_w <= 128 && units224 < 2 * sm_count();
+      if (mode == 5)
+        return narrow_c ? run<DT, true, false, 128, 1, 1, 128, false, false, true>(a, s, err)
+                        : run<DT, true, false, 224, 1, 1, 128, false, false, true>(a, s, err);
+      return narrow_c ? run<DT, false, false, 128, 1, 1, 128, false, false, true>(a, s, err)
+                      : run<DT, false, false, 224, 1, 1, 128, false, false, true>(a, s, err);
+    }
+    return cudaErrorInvalidValue;
   }
   // tile-wise and block-wise: 128-row tiles follow the pattern's tiles
   bool narrow = a.N <= 128 || a.nt * ceil_div(a.N, 256) < 2 * sm_count();

@@ -27,6 +27,8 @@ struct GemmArgs {
   const int32_t* offsets;
   const int32_t* indices;
   const int32_t* schedule;
+  // 3x3 convolution (implicit GEMM): NHWC activations, K = 9 C_in ordered (tap, channel)
+  int64_t conv_cin = 0, conv_h = 0, conv_w = 0, conv_nb = 0;
   // fused layer epilogue (out = round(y_scale * act(alpha * acc + bias[row])))
   const float* bias = nullptr;
   int act = 0;          // 0 none, 1 ReLU, 2 GELU
@@ -34,7 +36,8 @@ struct GemmArgs {
 };
 
 // mode: 0 dense, 1 sp24, 2 TW (dense packed + gather), 3 TVW (2:4 packed + gather),
-// 4 block-wise (dense packed blocks, X panels by TMA)
+// 4 block-wise (dense packed blocks, X panels by TMA), 5 / 6 3x3 convolution with a
+// 2:4 / dense filter (activation taps by 4-D TMA boxes of NHWC X)
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err);
 
 // Y = round(y_scale * act(bias[row])) for every element (the fused epilogue of a

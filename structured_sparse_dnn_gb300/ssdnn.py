@@ -64,6 +64,10 @@ _SIGS = {
     "ew_sizes": ([C.c_int, _i64, _i64, _i64, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "ew_prune_compress": ([C.c_int, _ptr, _i64, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], C.c_int),
     "ew_spmm": ([C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, _i64, _ptr, _i64, _ptr], C.c_int),
+    "sp24_conv3x3": ([C.c_int, C.c_int, _i64, _i64, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, _i64, C.c_float,
+                      _ptr], C.c_int),
+    "dense_conv3x3": ([C.c_int, C.c_int, _i64, _i64, _i64, _i64, _i64, _ptr, _i64, _ptr, _ptr, _i64, C.c_float,
+                       _ptr], C.c_int),
     "tw_sizes": ([C.c_int, C.c_int, _i64, _i64, _i32p, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz),
                   C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "tw_prune_compress": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
@@ -432,4 +436,26 @@ def ew_spmm(form: ElementWise, X: torch.Tensor, out: torch.Tensor | None = None)
     vals = form.val_buf if form.val_buf is not None else form.vals
     _check(lib.ew_spmm(form.dt, form.M, N, form.K, _p(form.row_ptr), _p(cols), _p(vals), _p(X),
                        X.stride(0), _p(out), out.stride(0), _stream(X.device)), "ew_spmm")
+    return out
+
+
+# ---------------------------------------------------------------- 3x3 convolution
+def conv3x3(filt, X: torch.Tensor, out: torch.Tensor | None = None, alpha: float = 1.0) -> torch.Tensor:
+    """3x3 convolution (stride 1, zero padding 1) of NHWC activations X (Nb, H, W, Cin).
+    `filt` is either an Sp24 (the 2:4 form of the Cout x 9 Cin flattened filter) or
+    the dense flattened filter tensor. Returns Y as Cout x (Nb H W)."""
+    Nb, H, W, Cin = X.shape
+    assert X.is_contiguous()
+    dt = _DT[X.dtype]
+    Cout = filt.M if isinstance(filt, Sp24) else filt.shape[0]
+    if out is None:
+        out = torch.empty((Cout, Nb * H * W), dtype=X.dtype, device=X.device)
+    if isinstance(filt, Sp24):
+        assert filt.K == 9 * Cin and filt.dt == dt
+        _check(lib.sp24_conv3x3(dt, _DT[out.dtype], Cout, Cin, Nb, H, W, _p(filt.values), _p(filt.meta_hw), _p(X),
+                                _p(out), out.stride(0), alpha, _stream(X.device)), "sp24_conv3x3")
+    else:
+        assert filt.shape[1] == 9 * Cin and filt.stride(1) == 1
+        _check(lib.dense_conv3x3(dt, _DT[out.dtype], Cout, Cin, Nb, H, W, _p(filt), filt.stride(0), _p(X), _p(out),
+                                 out.stride(0), alpha, _stream(X.device)), "dense_conv3x3")
     return out

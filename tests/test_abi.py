@@ -132,3 +132,11 @@ def test_bw_sizes_match_layout(ssdnn):
     # element-wise: k > K invalid, e4m3 unsupported
     assert ssdnn.lib.ew_sizes(1, 8, 16, 17, None, None, None) == 1
     assert ssdnn.lib.ew_sizes(2, 8, 16, 4, None, None, None) == 2
+
+
+def test_conv_argument_checks(ssdnn):
+    lib = ssdnn.lib
+    # C_in not a multiple of 64, image wider than 224, e4m3
+    assert lib.sp24_conv3x3(1, 1, 128, 32, 1, 8, 8, 16, 16, 16, 16, 64, 1.0, None) == 2
+    assert lib.sp24_conv3x3(1, 1, 128, 64, 1, 8, 256, 16, 16, 16, 16, 2048, 1.0, None) == 2
+    assert lib.dense_conv3x3(2, 1, 128, 64, 1, 8, 8, 16, 576, 16, 16, 64, 1.0, None) == 2

@@ -1,0 +1,40 @@
+"""GPU parity of the 3x3 convolution (implicit GEMM, stride 1, zero padding)
+through the C ABI, with a 2:4 and a dense filter, against the oracle's im2col
+convolution: small and ragged images (H not a multiple of the row patch, C_out
+not a multiple of 128), both N tile widths, and the ResNet-50 stage-3 shape."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import REL, bits_of, canary_intact, dev_tensor, guarded_output, lib, rand_bits
+
+pytestmark = pytest.mark.gpu
+
+# (Nb, H, W, Cin, Cout)
+CASES = [(1, 5, 7, 64, 128), (2, 14, 14, 128, 256), (1, 28, 28, 64, 200), (3, 9, 30, 64, 64), (1, 3, 224, 64, 128)]
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("sparse", [True, False])
+def test_conv3x3(dt, case, sparse):
+    ss = lib()
+    Nb, H, W, Cin, Cout = case
+    X = rand_bits(1100 + H + W, (Nb * H * W, Cin), dt, 1.0).reshape(Nb, H, W, Cin)
+    Wf = rand_bits(1110 + Cout + Cin, (Cout, 9 * Cin), dt, 0.2)
+    Xd = dev_tensor(X.reshape(-1, Cin), dt).reshape(Nb, H, W, Cin)
+    N = Nb * H * W
+    pad = 8 + (-N) % 8                                   # a 16-byte output pitch
+    Y, buf = guarded_output(Cout, N, torch.bfloat16 if dt == "bf16" else torch.float16, pad_cols=pad)
+    if sparse:
+        f = ss.sp24_prune_compress(dev_tensor(Wf, dt), canonical_meta=False)
+        ss.conv3x3(f, Xd, out=Y)
+    else:
+        ss.conv3x3(dev_tensor(Wf, dt), Xd, out=Y)
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
+    Y_ref, B = oracle.conv.conv3x3(Wf, X, dt, dt, sparse=sparse)
+    ok = oracle.gemm.within_bound(bits_of(Y), Y_ref, B, dt, REL[dt])
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outside the bound"
+    assert canary_intact(buf, Cout, N)
