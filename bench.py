@@ -458,6 +458,25 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
     dens = 128.0 * keep.sum() / (tw.M * tw.K)
     flops_tw = 2.0 * 128 * float(keep.sum()) * tw.N
     flops_tvw = 2.0 * 128 * float(keep4.sum()) * tw.N * 0.5
+    # 3x3 convolutions of ResNet-50 (NEXT-4), batch 32, 2:4 vs dense filter, implicit GEMM
+    conv_rows = {}
+    for (H, Cin, Cout) in ((28, 128, 128), (14, 256, 256)):
+        Nb = 32
+        g = np.random.default_rng(7)
+        Xc = torch.from_numpy(g.standard_normal((Nb, H, H, Cin)).astype(np.float32)).to(dev, torch.bfloat16)
+        Wc = torch.from_numpy((g.standard_normal((Cout, 9 * Cin)) * (2.0 / (9 * Cin)) ** 0.5).astype(np.float32)
+                              ).to(dev, torch.bfloat16)
+        fc = ss.sp24_prune_compress(Wc, canonical_meta=False)
+        Yc = torch.empty((Cout, Nb * H * H), dtype=torch.bfloat16, device=dev)
+        t_sp = statistics.mean(timed_steps(lambda: ss.conv3x3(fc, Xc, out=Yc), steps, 2, flush, stream))
+        t_dn = statistics.mean(timed_steps(lambda: ss.conv3x3(Wc, Xc, out=Yc), steps, 2, flush, stream))
+        flops = 2.0 * Cout * 9 * Cin * Nb * H * H
+        conv_rows[f"{H}x{H}x{Cin}->{Cout}, batch {Nb}"] = {
+            "sp24_ms": round(t_sp, 4), "dense_ms": round(t_dn, 4),
+            "sp24_effective_TFLOP/s": round(0.5 * flops / (t_sp * 1e-3) / 1e12, 1),
+            "dense_TFLOP/s": round(flops / (t_dn * 1e-3) / 1e12, 1), "speedup": round(t_dn / t_sp, 3)}
+        del Xc, Wc, fc, Yc
+    rows["conv3x3_resnet50"] = conv_rows
     rows["tile_wise"] = {
         "workload": tw.name, "kept_fraction": round(float(keep.sum()) / tw.K / len(keep), 4),
         "tw_prune_compress_ms (TVW)": round(t_prune, 4),
