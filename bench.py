@@ -269,11 +269,23 @@ def run_gpu(args) -> None:
     copy_stream = torch.cuda.Stream(device=dev)
     e2e_rows = 2048
 
-    def e2e_step():
+    def e2e_copies():
         ss.sp24_gemm_host(form, X_host, Y_host, Xd, Y, alpha=alpha, rows_per_block=e2e_rows, copy_stream=copy_stream)
 
-    e2e_times = timed_steps(e2e_step, max(3, args.steps // 2), 2, flush, stream)
-    e2e_value = ws * eff_flops / (statistics.mean(e2e_times) * 1e-3) / 1e12
+    def e2e_direct():  # the epilogue stores Y into the pinned host buffer itself
+        ss.sp24_gemm_host(form, X_host, Y_host, Xd, None, alpha=alpha)
+
+    e2e_paths = {
+        "copies": (e2e_copies, f"sp24_gemm_host (pinned host X and Y, {e2e_rows}-row blocks, "
+                               "device Y copied out on a second stream)"),
+        "direct": (e2e_direct, "sp24_gemm_host (pinned host X and Y, X copied in, the epilogue stores Y "
+                               "into host memory)"),
+    }
+    e2e_ms = {}
+    for key, (fn, _) in e2e_paths.items():
+        e2e_ms[key] = statistics.mean(timed_steps(fn, max(3, args.steps // 2), 2, flush, stream))
+    e2e_best = min(e2e_ms, key=e2e_ms.get)
+    e2e_value = ws * eff_flops / (e2e_ms[e2e_best] * 1e-3) / 1e12
 
     rows = {}
     mma = None
@@ -301,8 +313,8 @@ def run_gpu(args) -> None:
                          "peak_note": f"2:4-sparse {wl.dt} peak in nonzero-MAC TFLOP/s = "
                                       f"{'2 x ' if wl.dt == 'e4m3' else ''}{pk['source']} bf16 dense burst "
                                       f"{pk['bf16_tflops']}"},
-            "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
-                    "path": f"sp24_gemm_host (pinned host X and Y, {e2e_rows}-row blocks, copies overlapped)",
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "path": e2e_paths[e2e_best][1],
+                    "ms_per_step": {k: round(v, 4) for k, v in e2e_ms.items()},
                     "h2d_bytes_per_step": int(Xd.numel() * Xd.element_size()),
                     "d2h_bytes_per_step": int(Y.numel() * Y.element_size())},
             "mma_microbench_dense_equivalent_tflops": mma,

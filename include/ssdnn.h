@@ -182,7 +182,12 @@ int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* ke
  * on `stream`, in order). The host buffers should be page-locked for the copies
  * to be asynchronous. The call only enqueues; Y_host is complete once `stream`
  * has completed. Returns as sp24_gemm, or SSDNN_ERR_INVALID_ARG for a null host
- * buffer or a block height that is not a multiple of 128. */
+ * buffer or a block height that is not a multiple of 128.
+ * Y_dev NULL: the GEMM's epilogue stores the result straight into Y_host, which
+ * must then be page-locked (cudaHostAlloc / cudaHostRegister; anything else is
+ * SSDNN_ERR_INVALID_ARG); rows_per_block and copy_stream are ignored and K = 0 is
+ * SSDNN_ERR_UNSUPPORTED. The product path refuses host memory for every other
+ * operand. */
 int sp24_gemm_host(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
                    const uint8_t* meta_hw, const void* X_host, int64_t ldx, void* Y_host, int64_t ldy, float alpha,
                    void* X_dev, void* Y_dev, int64_t rows_per_block, void* stream, void* copy_stream);

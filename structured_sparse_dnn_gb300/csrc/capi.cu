@@ -66,7 +66,10 @@ bool valid_dt(int dt) { return dt == SSDNN_F16 || dt == SSDNN_BF16 || dt == SSDN
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
-int from_cuda(cudaError_t e) { return e == cudaSuccess ? SSDNN_OK : SSDNN_ERR_CUDA; }
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return SSDNN_OK;
+  return e == cudaErrorInvalidValue ? SSDNN_ERR_INVALID_ARG : SSDNN_ERR_CUDA;
+}
 
 int out_bytes(int out_dt) { return out_dt == SSDNN_E4M3 ? 1 : 2; }
 
@@ -423,9 +426,11 @@ int sp24_gemm_host(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const
                    void* X_dev, void* Y_dev, int64_t rows_per_block, void* stream, void* copy_stream) {
   if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
   const int eb = elem_bytes(in_dt);
-  int st = check_gemm_io(out_dt, false, M, N, K, X_dev, ldx, eb, Y_dev, ldy);
+  const bool direct = Y_dev == nullptr;  // the epilogue writes the page-locked Y_host itself
+  int st = check_gemm_io(out_dt, false, M, N, K, X_dev, ldx, eb, direct ? Y_host : Y_dev, ldy);
   if (st != SSDNN_OK || M == 0 || N == 0) return st;
   if (!Y_host || (K > 0 && !X_host)) return SSDNN_ERR_INVALID_ARG;
+  if (direct && K == 0) return SSDNN_ERR_UNSUPPORTED;
   if (rows_per_block < 0 || rows_per_block % 128) return SSDNN_ERR_INVALID_ARG;
   if (K % 4) return SSDNN_ERR_UNSUPPORTED;
   auto s = static_cast<cudaStream_t>(stream);
@@ -438,6 +443,9 @@ int sp24_gemm_host(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const
                           cudaMemcpyHostToDevice, s) != cudaSuccess)
       return SSDNN_ERR_CUDA;
   }
+  if (direct)
+    return sp24_gemm_impl(in_dt, out_dt, M, N, K, values, meta_hw, X_dev, ldx, Y_host, ldy, alpha, nullptr, false,
+                          stream);
   const int64_t rb = rows_per_block > 0 ? rows_per_block : M;
   const int64_t Kp = round_up(K, 32), KB = ceil_div(K, in_dt == SSDNN_E4M3 ? 128 : 64);
   for (int64_t r0 = 0; r0 < M; r0 += rb) {

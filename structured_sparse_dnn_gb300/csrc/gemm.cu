@@ -74,6 +74,7 @@ struct Params {
   int32_t conv_cin, conv_h, conv_w, conv_rows;  // C_in, H, W, image rows per patch
   int32_t conv_patches;                         // patches per image
   uint32_t conv_box_bytes;                      // bytes one activation box delivers
+  int32_t y_direct;                             // Y is page-locked host memory: plain stores, no TMA
 };
 
 template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128, bool PAIR = false,
@@ -731,6 +732,10 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
         uint32_t w[16];
         pack_row32(p.out_dt, x, w);
         if constexpr (C::STAGED) {
+          if (p.y_direct) {  // host-memory output: each thread stores its row's chunk
+            if (row_ok && n0 < p.N) store_packed_row32(yrow, n0, p.N, p.out_dt, w, pol_y);
+            continue;
+          }
           // this warp's 32 rows x 32 columns go through a staging buffer and a TMA
           // store, which clips rows past M and columns past N
           if (ui.phantom || wrow0 >= p.M || n0 >= p.N) continue;  // uniform over the warp
@@ -886,8 +891,28 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   } else {
     tM = tA;  // unused
   }
+  // Y in page-locked host memory is written by plain stores from the epilogue (the
+  // copy engine is not used on host memory); other host memory is refused.
+  bool y_host = false;
+  {
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, a.Y) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return cudaErrorInvalidValue;
+    }
+    if (attr.type == cudaMemoryTypeUnregistered) return cudaErrorInvalidValue;
+    y_host = attr.type == cudaMemoryTypeHost;
+    for (const void* in : {a.A, a.X, static_cast<const void*>(a.meta_hw)}) {
+      if (!in) continue;
+      if (cudaPointerGetAttributes(&attr, in) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return cudaErrorInvalidValue;
+      }
+      if (attr.type == cudaMemoryTypeHost || attr.type == cudaMemoryTypeUnregistered) return cudaErrorInvalidValue;
+    }
+  }
   CUtensorMap tY;
-  if constexpr (C::STAGED) {
+  if (C::STAGED && !y_host) {
     // the output as 32 x 32 boxes (64-byte rows with the 64B swizzle; e4m3: 32-byte rows, 32B swizzle)
     const bool f8_out = a.out_dt == SSDNN_E4M3;
     ok = ok && make_map(&tY, a.Y, f8_out ? 1 : 2, a.N, a.M, a.ldy * (f8_out ? 1 : 2), 32, 32,
@@ -939,6 +964,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.Y = static_cast<uint8_t*>(a.Y);
   p.ldy = a.ldy;
   p.err = err;
+  p.y_direct = y_host ? 1 : 0;
   if (p.num_units == 0) return cudaSuccess;
 
   auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>;

@@ -200,19 +200,21 @@ def sp24_gemm(form: Sp24, X: torch.Tensor, out_dtype: torch.dtype | None = None,
 
 
 def sp24_gemm_host(form: Sp24, X_host: torch.Tensor, Y_host: torch.Tensor, X_dev: torch.Tensor,
-                   Y_dev: torch.Tensor, alpha: float = 1.0, rows_per_block: int = 0,
+                   Y_dev: torch.Tensor | None, alpha: float = 1.0, rows_per_block: int = 0,
                    copy_stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """Y_host = alpha * decompress(form) . X_host through the device buffers X_dev and
     Y_dev, the copies of Y overlapped with the GEMM of later row blocks when a
-    copy stream is given. Enqueues only: Y_host is complete once the current stream is."""
+    copy stream is given; with Y_dev None the GEMM stores into the pinned Y_host
+    itself. Enqueues only: Y_host is complete once the current stream is."""
     dt = _DT[X_host.dtype]
-    assert dt == form.dt and X_host.shape == X_dev.shape and Y_host.shape == Y_dev.shape
-    assert X_host.stride(0) == X_dev.stride(0) and Y_host.stride(0) == Y_dev.stride(0)
+    assert dt == form.dt and X_host.shape == X_dev.shape and X_host.stride(0) == X_dev.stride(0)
+    assert Y_dev is None or (Y_host.shape == Y_dev.shape and Y_host.stride(0) == Y_dev.stride(0))
     N = X_host.shape[1]
     cs = copy_stream.cuda_stream if copy_stream is not None else None
     _check(lib.sp24_gemm_host(dt, _DT[Y_host.dtype], form.M, N, form.K, _p(form.values), _p(form.meta_hw),
                               X_host.data_ptr(), X_host.stride(0), Y_host.data_ptr(), Y_host.stride(0), alpha,
-                              _p(X_dev), _p(Y_dev), rows_per_block, _stream(X_dev.device), cs), "sp24_gemm_host")
+                              _p(X_dev), None if Y_dev is None else _p(Y_dev), rows_per_block,
+                              _stream(X_dev.device), cs), "sp24_gemm_host")
     return Y_host
 
 

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (REL, bits_of, canary_intact, dev_padded, dev_tensor, guarded_output, lib,
+from gpu_helpers import (CANARY, REL, bits_of, canary_intact, dev_padded, dev_tensor, guarded_output, lib,
                          rand_bits)
 
 pytestmark = pytest.mark.gpu
@@ -222,6 +222,61 @@ def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
         assert ss.check_device_error() == 0, tile
         _check_y(Y, Y_ref, B, out_dt, REL[dt])
         assert canary_intact(buf, M, N), tile
+
+
+@pytest.mark.parametrize("dt", ["bf16", "e4m3"])
+@pytest.mark.parametrize("tile", [None, "1128", "9256"])
+def test_sp24_gemm_host_direct_output(dt, tile, monkeypatch):
+    """Y_dev None: the epilogue stores straight into page-locked host memory. The
+    result is bit-identical to the same tiles' device output, and nothing outside
+    the M x N view of the pinned buffer is written."""
+    ss = lib()
+    if tile:
+        monkeypatch.setenv("SSDNN_TILE", tile)
+    M, N, K = 1000, 264, 512
+    W = rand_bits(811, (M, K), dt, 0.5)
+    X = rand_bits(812, (K, N), dt, 1.0)
+    f = ss.sp24_prune_compress(dev_tensor(W, dt), canonical_meta=False)
+    Xd = dev_padded(X, dt)
+    X_host = Xd.cpu().pin_memory()
+    X_dev = torch.empty_like(Xd)
+    out = torch.bfloat16
+    Y_dev = torch.empty((M, N), dtype=out, device="cuda")
+    ss.sp24_gemm(f, Xd, alpha=0.5, out=Y_dev)
+    buf = torch.empty((M + 2, N + 8), dtype=out).pin_memory()
+    buf.view(torch.uint8).fill_(CANARY)
+    Y_host = buf[:M, :N]
+    ss.sp24_gemm_host(f, X_host, Y_host, X_dev, None, alpha=0.5)
+    torch.cuda.current_stream().synchronize()
+    assert ss.check_device_error() == 0
+    assert np.array_equal(bits_of(Y_host), bits_of(Y_dev))
+    b = buf.view(torch.uint8).numpy().reshape(M + 2, -1)
+    assert (b[:M, 2 * N:] == CANARY).all() and (b[M:] == CANARY).all()
+    v_ref, m_ref = oracle.sp24.compress(W, dt)
+    Y_ref = oracle.gemm.gemm_sp24(v_ref, m_ref, K, X, dt, "bf16", 0.5)
+    B = oracle.gemm.bound(oracle.sp24.decompress(v_ref, m_ref, K), X, dt, 0.5)
+    _check_y(Y_host, Y_ref, B, "bf16", REL[dt])
+
+
+def test_host_memory_operands_refused():
+    """Pageable host memory as the direct output, or host memory as an input of the
+    device GEMM, is refused on the host before anything is launched."""
+    ss = lib()
+    M, N, K = 256, 128, 256
+    W = rand_bits(821, (M, K), "bf16", 0.5)
+    X = rand_bits(822, (K, N), "bf16", 1.0)
+    f = ss.sp24_prune_compress(dev_tensor(W, "bf16"), canonical_meta=False)
+    Xd = dev_tensor(X, "bf16")
+    X_host = Xd.cpu().pin_memory()
+    with pytest.raises(ss.SsdnnError) as e:
+        ss.sp24_gemm_host(f, X_host, torch.empty((M, N), dtype=torch.bfloat16), torch.empty_like(Xd), None)
+    assert e.value.status == 1
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = ss.lib.sp24_gemm(ss.BF16, ss.BF16, M, N, K, f.values.data_ptr(), f.meta_hw.data_ptr(), X_host.data_ptr(),
+                          N, Y.data_ptr(), N, 1.0, torch.cuda.current_stream().cuda_stream)
+    assert st == 1
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
 
 
 @pytest.mark.parametrize("copy_stream", [False, True])
