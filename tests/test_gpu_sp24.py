@@ -238,8 +238,11 @@ def test_sp24_gemm_host_direct_output(dt, tile, monkeypatch):
     X = rand_bits(812, (K, N), dt, 1.0)
     f = ss.sp24_prune_compress(dev_tensor(W, dt), canonical_meta=False)
     Xd = dev_padded(X, dt)
-    X_host = Xd.cpu().pin_memory()
-    X_dev = torch.empty_like(Xd)
+    ld = Xd.stride(0)                       # rows padded to 16 bytes, as the GEMM requires
+    X_host = torch.empty((K, ld), dtype=Xd.dtype).pin_memory()
+    X_host.copy_(Xd.as_strided((K, ld), (ld, 1)))
+    X_host = X_host[:, :N]
+    X_dev = torch.empty((K, ld), dtype=Xd.dtype, device="cuda")[:, :N]
     out = torch.bfloat16
     Y_dev = torch.empty((M, N), dtype=out, device="cuda")
     ss.sp24_gemm(f, Xd, alpha=0.5, out=Y_dev)
