@@ -193,6 +193,21 @@ def mma_microbench(ss, stream) -> dict:
                     ts.append(a.elapsed_time(b))
                 flops = sms * iters * 2.0 * 128 * n * (128 // eb)
                 out[f"{dname}_{'sparse' if sparse else 'dense'}_n{n}"] = round(flops / (min(ts) * 1e-3) / 1e12, 1)
+        for sparse in (False, True):  # SM pairs, M = 256, N = 256 (the large GEMM tiles' instruction)
+            iters = 16384
+            ss.mma_rate_pair(dt, sparse, iters)
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(3):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                ss.mma_rate_pair(dt, sparse, iters)
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b))
+            flops = (sms // 2) * iters * 2.0 * 256 * 256 * (128 // eb)
+            out[f"{dname}_{'sparse' if sparse else 'dense'}_pair_n256"] = round(flops / (min(ts) * 1e-3) / 1e12, 1)
     assert ss.check_device_error() == 0, "device error flag set by the MMA microbenchmark"
     return out
 
@@ -322,10 +337,11 @@ def run_gpu(args) -> None:
             "clocks": clocks,
             "rows": rows,
         }
-        key = f"{wl.dt}_sparse_n192"
+        key = f"{wl.dt}_sparse_pair_n256"
         if mma and key in mma:
             # the same ceiling as measured on chip at the headline's instruction shape
-            # (effective = dense-equivalent / 2)
+            # (SM pairs, M = 256, N = 256, one metadata copy per K stage;
+            # effective = dense-equivalent / 2)
             mb = mma[key] / 2.0
             line["roofline"]["peak_sparse_mma_microbench"] = round(mb, 1)
             line["roofline"]["frac_of_microbench"] = round(achieved / mb, 4)

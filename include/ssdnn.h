@@ -89,6 +89,16 @@ int ssdnn_selftest_wait_timeout(uint32_t limit_us, void* stream);
  * step count or n, else the launch status. */
 int ssdnn_mma_rate(int dt, int sparse, int n, int iters, void* stream);
 
+/* The same measurement on SM pairs (tcgen05 cta_group::2, the form the large GEMM
+ * tiles use): clusters of two CTAs on an even number of SMs, M = 256, N = 256,
+ * 128 bytes of K per step; each CTA holds 128 rows of A and 128 columns of B. In
+ * the 2:4 form every step also copies its 128 x 16-byte metadata block into TMEM
+ * before its instructions, as the GEMM does for each K stage. A step is
+ * 2 * 256 * 256 * (128 / elem bytes) dense-equivalent flops per pair. Returns
+ * SSDNN_ERR_INVALID_ARG for a bad dtype, flag or step count, else the launch
+ * status. */
+int ssdnn_mma_rate_pair(int dt, int sparse, int iters, void* stream);
+
 /* ------------------------------------------------------------------ 2:4 ----
  * Compressed 2:4 layouts (Kp = round_up(K, 32)):
  *   values   M x Kp/2 elements, row-major: the kept values of each group in

@@ -376,6 +376,14 @@ int ssdnn_mma_rate(int dt, int sparse, int n, int iters, void* stream) {
   return from_cuda(launch_mma_rate(dt, sparse, n, iters, static_cast<cudaStream_t>(stream), w));
 }
 
+int ssdnn_mma_rate_pair(int dt, int sparse, int iters, void* stream) {
+  if (!valid_dt(dt) || (sparse != 0 && sparse != 1) || iters < 1 || iters > (1 << 18))
+    return SSDNN_ERR_INVALID_ARG;
+  uint32_t* w = error_word();
+  if (!w) return SSDNN_ERR_CUDA;
+  return from_cuda(launch_mma_rate_pair(dt, sparse, iters, static_cast<cudaStream_t>(stream), w));
+}
+
 int ssdnn_selftest_wait_timeout(uint32_t limit_us, void* stream) {
   if (limit_us == 0 || limit_us > 1000000u) return SSDNN_ERR_INVALID_ARG;
   uint32_t* w = error_word();

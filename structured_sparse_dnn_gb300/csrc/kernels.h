@@ -72,5 +72,6 @@ cudaError_t launch_ew_spmm(int dt, int64_t M, int64_t N, int64_t K, const int32_
 
 // Tensor-core issue-rate microbenchmark (operands resident on chip), one CTA per SM.
 cudaError_t launch_mma_rate(int dt, int sparse, int n, int iters, cudaStream_t s, uint32_t* err);
+cudaError_t launch_mma_rate_pair(int dt, int sparse, int iters, cudaStream_t s, uint32_t* err);
 
 }  // namespace ssdnn

@@ -42,6 +42,7 @@ _SIGS = {
     "ssdnn_check_device_error": ([_ptr], C.c_int),
     "ssdnn_selftest_wait_timeout": ([C.c_uint32, _ptr], C.c_int),
     "ssdnn_mma_rate": ([C.c_int, C.c_int, C.c_int, C.c_int, _ptr], C.c_int),
+    "ssdnn_mma_rate_pair": ([C.c_int, C.c_int, C.c_int, _ptr], C.c_int),
     "sp24_sizes": ([C.c_int, _i64, _i64, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "sp24_prune_compress": ([C.c_int, _ptr, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], C.c_int),
     "sp24_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _i64, _ptr, _i64, C.c_float, _ptr],
@@ -126,6 +127,13 @@ def mma_rate(dt: int, sparse: bool, n: int, iters: int, stream: int | None = Non
     steps of 2 * 128 * n * (128 / elem bytes) dense-equivalent flops each)."""
     _check(lib.ssdnn_mma_rate(dt, int(sparse), n, iters, stream if stream is not None else _stream(None)),
            "ssdnn_mma_rate")
+
+
+def mma_rate_pair(dt: int, sparse: bool, iters: int, stream: int | None = None) -> None:
+    """The microbenchmark on SM pairs (M = 256, N = 256 per pair; `iters` steps of
+    2 * 256 * 256 * (128 / elem bytes) dense-equivalent flops per pair)."""
+    _check(lib.ssdnn_mma_rate_pair(dt, int(sparse), iters, stream if stream is not None else _stream(None)),
+           "ssdnn_mma_rate_pair")
 
 
 def selftest_wait_timeout(limit_us: int = 1000, stream: int | None = None) -> None:

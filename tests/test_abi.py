@@ -102,6 +102,10 @@ def test_argument_errors_before_any_device_work(ssdnn):
     assert lib.ssdnn_mma_rate(7, 0, 128, 16, None) == 1
     assert lib.ssdnn_mma_rate(1, 2, 128, 16, None) == 1
     assert lib.ssdnn_mma_rate(1, 0, 128, 0, None) == 1
+    assert lib.ssdnn_mma_rate_pair(7, 0, 16, None) == 1
+    assert lib.ssdnn_mma_rate_pair(1, 2, 16, None) == 1
+    assert lib.ssdnn_mma_rate_pair(1, 0, 0, None) == 1
+    assert lib.ssdnn_mma_rate_pair(2, 1, (1 << 18) + 1, None) == 1
     assert lib.ssdnn_mma_rate(1, 0, 96, 16, None) == 2
     # fused epilogue: unknown activation, non-finite scale, misaligned bias, e4m3 pitch
     import ctypes as C

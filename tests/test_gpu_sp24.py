@@ -176,6 +176,7 @@ def test_mma_rate_microbenchmark_runs_clean(dt, sparse):
     ss = lib()
     for n in (128, 192, 256):
         ss.mma_rate(ss.BF16 if dt == "bf16" else ss.E4M3, sparse, n, 64)
+    ss.mma_rate_pair(ss.BF16 if dt == "bf16" else ss.E4M3, sparse, 64)
     torch.cuda.synchronize()
     assert ss.check_device_error() == 0
 
