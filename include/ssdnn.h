@@ -197,7 +197,9 @@ int tvw_gemm(int dt, int tvw, int64_t M, int64_t N, int64_t K, const int32_t* ke
  * must then be page-locked (cudaHostAlloc / cudaHostRegister; anything else is
  * SSDNN_ERR_INVALID_ARG); rows_per_block and copy_stream are ignored and K = 0 is
  * SSDNN_ERR_UNSUPPORTED. The product path refuses host memory for every other
- * operand. */
+ * operand. The direct form saves the device buffer, not time: the epilogue's
+ * row-wise stores cross the host link in small transactions, several times
+ * slower than the copy engines for a large Y. */
 int sp24_gemm_host(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
                    const uint8_t* meta_hw, const void* X_host, int64_t ldx, void* Y_host, int64_t ldy, float alpha,
                    void* X_dev, void* Y_dev, int64_t rows_per_block, void* stream, void* copy_stream);

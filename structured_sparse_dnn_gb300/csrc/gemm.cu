@@ -55,6 +55,7 @@ struct Params {
   int32_t GR;               // rasterisation: M groups per band; work sweeps a band's N blocks
   int32_t num_units;        // work items: (M group, N block) pairs, or (schedule entry, N block)
   int32_t nk;               // k stages per unit (dense / sp24)
+  int32_t meta_kb;          // 2048-byte metadata blocks per 128-row block (one per 128 bytes of K)
   int32_t out_dt;           // 0 f16, 1 bf16, 2 e4m3
   int32_t act;              // fused epilogue: 0 none, 1 ReLU, 2 GELU
   const float* bias;        // fused epilogue: one fp32 bias per output row, or null
@@ -78,7 +79,7 @@ struct Params {
 };
 
 template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128, bool PAIR = false,
-          bool BLOCKW = false, bool CONV = false>
+          bool BLOCKW = false, bool CONV = false, int KX = 1>
 struct Cfg {
   // CONV: 3x3 convolution as an implicit GEMM -- the B operand of a K stage is one
   // tap (r, s) and 64 input channels of a patch of image rows, loaded K-major by one
@@ -114,11 +115,14 @@ struct Cfg {
   static constexpr int GATHER_LAG = STAGES_FOR_LAG >= 8 ? 2 : 1;
   static constexpr int EB = Elem<DT>::bytes;
   static constexpr bool F8 = Elem<DT>::f8;
-  static constexpr int BK = 128 / EB;                       // dense K per stage
-  static constexpr int A_SUB_BYTES = SPARSE ? 128 * 64 : 128 * 128;
+  // KX = 2 (2:4 on SM pairs): a stage holds two 128-byte K steps, so every
+  // compressed weight row of the stage is one 128-byte (128B-swizzled) row and the
+  // ring turns over half as often
+  static constexpr int BK = KX * 128 / EB;                  // dense K per stage
+  static constexpr int A_SUB_BYTES = KX * (SPARSE ? 128 * 64 : 128 * 128);
   static constexpr int A_BYTES = MT * A_SUB_BYTES;
-  static constexpr int B_BYTES = 128 * BN_CTA;              // BK * BN_CTA * EB
-  static constexpr int META_BYTES = SPARSE ? 2048 * MT : 0;
+  static constexpr int B_BYTES = KX * 128 * BN_CTA;         // BK * BN_CTA * EB
+  static constexpr int META_BYTES = SPARSE ? 2048 * MT * KX : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + META_BYTES;
   // Output staging (all but TW/TVW): each epilogue warp converts a 32 x 32 chunk
   // into one of two 2 KB shared-memory buffers and a TMA store writes it out, so
@@ -140,7 +144,7 @@ struct Cfg {
   static_assert(BROW == 128 || (BROW == 64 && !GATHER), "the gather writes 128-byte rows");
   static constexpr int ACC_COLS = MT * BN;                  // fp32 accumulator columns of one tile
   static constexpr int META_SLOTS = 4;
-  static constexpr int META_SLOT_COLS = 4 * MT;             // one 128x128b copy per sub-tile
+  static constexpr int META_SLOT_COLS = 4 * MT * KX;        // one 128x128b copy per sub-tile and K step
   static constexpr int META_COLS = SPARSE ? META_SLOTS * META_SLOT_COLS : 0;
   static constexpr int NACC = (2 * ACC_COLS + META_COLS <= 512) ? 2 : 1;
   static constexpr int META_COL0 = NACC * ACC_COLS;         // TMEM columns after the accumulators
@@ -156,6 +160,7 @@ struct Cfg {
   static_assert(!CONV || (!GATHER && !PAIR && !BLOCKW && MT == 1 && CS == 1 && Elem<DT>::bytes == 2),
                 "convolution: 16-bit, 128-row tiles");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
+  static_assert(KX == 1 || (KX == 2 && SPARSE && PAIR), "double K stages: 2:4 on SM pairs");
   static_assert(MT == 1 || (CS == 1 && !GATHER), "256-row tiles: no cluster, no gather");
   static_assert(CS == 1 || !GATHER, "gathered B rows differ per tile: no multicast");
   static constexpr int B_SLICE_ROWS = BK / (MCAST ? CS : 1); // rows of each B box this CTA loads
@@ -216,8 +221,8 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
     ui.n0 = nb * BN_OF<C>();
     ui.nk = p.nk;
     ui.a_row0 = ui.m0;
-    // one 2048-byte metadata block per (128-row block, stage)
-    ui.meta_blk0 = mb * C::SUB * p.nk;
+    // one 2048-byte metadata block per (128-row block, 128 bytes of K)
+    ui.meta_blk0 = mb * C::SUB * p.meta_kb;
     ui.subs = ui.phantom ? 0 : min(C::SUB, p.MB128 - mb * C::SUB);
     ui.idx_base = 0;
     ui.L = 0;
@@ -328,11 +333,12 @@ __device__ __forceinline__ void stage_packed_row32(uint8_t* buf, uint32_t lane, 
         make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR, bool BLOCKW, bool CONV>
-__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>::THREADS, 1)
+template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR, bool BLOCKW, bool CONV,
+          int KX>
+__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>;
   // Multicast clusters (CS CTAs along M) share each X panel: CTA rank r loads rows
   // [r BK/CS, (r+1) BK/CS) of every B box of a stage and multicasts them to the
   // whole cluster, so a stage is complete only when all CS slices have landed and
@@ -367,7 +373,10 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
   uint64_t* acc_full = bars + 2 * C::STAGES;
   uint64_t* acc_empty = acc_full + C::NACC;
   uint64_t* drain = acc_empty + C::NACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  // KX = 2: the X boxes of a stage complete on a second barrier, so that neither
+  // barrier expects more than 64 KB per phase
+  uint64_t* full_b = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full_b + (KX == 2 ? C::STAGES : 0));
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const uint32_t warp = threadIdx.x >> 5;
@@ -377,6 +386,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(&full[s], 1 + C::GATHER_THREADS);
       ptx::mbar_init(&empty[s], C::MCAST ? CS : 1);
+      if constexpr (KX == 2) ptx::mbar_init(&full_b[s], 1);
     }
     for (int a = 0; a < C::NACC; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
@@ -429,17 +439,19 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
         if (lane == 0) {
           if constexpr (PAIR) {
             // both CTAs' bytes complete on the even CTA's full barrier
-            constexpr uint32_t kTx = 2u * (C::A_BYTES + C::B_BYTES + (SPARSE ? 2048u : 0u));
+            constexpr uint32_t kTx = 2u * (C::A_BYTES + (KX == 2 ? 0 : C::B_BYTES) + C::META_BYTES);
             if (leader) ptx::mbar_arrive_expect_tx(&full[stage], kTx);
+            if (KX == 2 && leader) ptx::mbar_arrive_expect_tx(&full_b[stage], 2u * C::B_BYTES);
             const uint32_t bar = ptx::mapa(ptx::smem_u32(&full[stage]), crank & ~1u);
+            const uint32_t bar_b = KX == 2 ? ptx::mapa(ptx::smem_u32(&full_b[stage]), crank & ~1u) : bar;
             ptx::tma_load_2d_pair(sA, &tmA, bar, kb * (SPARSE ? C::BK / 2 : C::BK), ui.m0, pol_a);
             if constexpr (SPARSE)  // one metadata block; past the last row block it reads zeros
-              ptx::tma_load_2d_pair(sM, &tmM, bar, 0, (ui.meta_blk0 + kb) * 16, pol_a);
+              ptx::tma_load_2d_pair(sM, &tmM, bar, 0, (ui.meta_blk0 + KX * kb) * 16, pol_a);
             const int32_t n_half = ui.n0 + static_cast<int32_t>(crank & 1u) * C::BN_CTA;
 #pragma unroll
             for (int bx = 0; bx < C::B_BOXES; ++bx)
-              ptx::tma_load_2d_pair(sB + bx * C::B_BOX_BYTES, &tmB, bar, n_half + bx * C::B_BOX_COLS, kb * C::BK,
-                                    pol_b);
+              ptx::tma_load_2d_pair(sB + bx * C::B_BOX_BYTES, &tmB, bar_b, n_half + bx * C::B_BOX_COLS,
+                                    kb * C::BK, pol_b);
           } else {
           ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0u : (CONV ? p.conv_box_bytes : C::B_BYTES)) +
                                                        (SPARSE ? 2048 * ui.subs : 0));
@@ -503,6 +515,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
       for (int n = 0; n < pending; ++n) {
         if (--s < 0) { s = p.nstages - 1; ph ^= 1u; }
         wait_bounded(&full[s], ph, nullptr);
+        if constexpr (KX == 2) wait_bounded(&full_b[s], ph, nullptr);
       }
     }
   } else if (warp == 1 && leader) {
@@ -524,6 +537,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
       uint32_t cur_meta = 0;
       for (int32_t kb = 0; kb < ui.nk; ++kb) {
         if (lane == 0) ok = wait_bounded(&full[stage], phase, p.err);
+        if (KX == 2 && lane == 0 && ok) ok = wait_bounded(&full_b[stage], phase, p.err);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) { *abort_flag = 1; break; }
         ptx::tc_fence_after();
@@ -536,7 +550,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
             meta_slot = (meta_slot + 1) % C::META_SLOTS;
             // per sub-tile: 128 rows x 16 B, rows contiguous (8-row core matrices 128 B apart)
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
+            for (int mt = 0; mt < MT * KX; ++mt) {  // sub-tiles, or (KX = 2) the stage's two K steps
               if constexpr (PAIR)  // each CTA's block into its own TMEM
                 ptx::tmem_cp_128x128b_pair(cur_meta + 4u * mt, ptx::sdesc(sM + 2048u * mt, 128, 128, 0));
               else
@@ -554,11 +568,13 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
             const uint32_t d_sub = d_tmem + static_cast<uint32_t>(mt * BN);
             const uint32_t a_sub = sA + static_cast<uint32_t>(mt * C::A_SUB_BYTES);
             if constexpr (SPARSE) {
-              const uint64_t adesc = ptx::sdesc(a_sub + j * 32, 16, 512, 4);
-              // the metadata of instruction j starts at column 2 j of the stage's four
-              // (the sparse MMA reads it from an even column: one column for a
+              // 64-byte rows, 64B swizzle; (KX = 2) 128-byte rows, 128B swizzle
+              const uint64_t adesc = KX == 1 ? ptx::sdesc(a_sub + j * 32, 16, 512, 4)
+                                             : ptx::sdesc(a_sub + j * 32, 16, 1024, 2);
+              // the metadata of instruction j starts at column 2 j of the stage's
+              // 4 KX (the sparse MMA reads it from an even column: one column for a
               // 16-bit K = 32 step, two for an e4m3 K = 64 step)
-              const uint32_t col = 4u * mt + 2u * j;
+              const uint32_t col = 4u * KX * mt + 2u * j;
               if constexpr (PAIR && C::F8)
                 ptx::mma_sp_f8_pair(d_sub, adesc, bdesc, cur_meta + col, C::IDESC, accum);
               else if constexpr (PAIR)
@@ -843,9 +859,9 @@ int sm_count() {
 }
 
 template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128, bool PAIR = false,
-          bool BLOCKW = false, bool CONV = false>
+          bool BLOCKW = false, bool CONV = false, int KX = 1>
 cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>;
   const int eb = C::EB;
   CUtensorMap tA, tB, tM;
   bool ok;
@@ -868,7 +884,10 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::B_SLICE_ROWS,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   } else if constexpr (!GATHER) {
-    if constexpr (SPARSE)
+    if constexpr (SPARSE && KX == 2)
+      ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 128 / eb, C::BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    else if constexpr (SPARSE)
       ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, C::BM,
                     CU_TENSOR_MAP_SWIZZLE_64B);
     else
@@ -886,8 +905,8 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   if constexpr (PAIR && SPARSE) {
     // the 2048-byte metadata blocks as a (blocks * 16) x 128-byte matrix: one 16-row
     // box per stage (long rows: the copy engine's cost grows with the rows of a box)
-    const uint64_t rows = static_cast<uint64_t>(ceil_div(a.M, 128)) * ceil_div(a.K, C::BK) * 16;
-    ok = ok && make_map(&tM, a.meta_hw, 1, 128, rows, 128, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const uint64_t rows = static_cast<uint64_t>(ceil_div(a.M, 128)) * ceil_div(a.K, 128 / eb) * 16;
+    ok = ok && make_map(&tM, a.meta_hw, 1, 128, rows, 128, 128, 16 * KX, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     tM = tA;  // unused
   }
@@ -935,6 +954,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     p.GR = static_cast<int32_t>(ceil_div(p.MG, bands));
   }
   p.nk = static_cast<int32_t>(ceil_div(a.K, C::BK));
+  p.meta_kb = static_cast<int32_t>(ceil_div(a.K, 128 / eb));
   p.num_units = C::SCHEDULED ? static_cast<int32_t>(a.nt) * p.NB : p.MG * p.NB;
   if constexpr (CONV) {
     p.conv_cin = static_cast<int32_t>(a.conv_cin);
@@ -967,7 +987,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.y_direct = y_host ? 1 : 0;
   if (p.num_units == 0) return cudaSuccess;
 
-  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV>;
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   constexpr int CL = C::CLUSTER;
@@ -1063,12 +1083,22 @@ int tile_override() {
   return e ? atoi(e) : 0;
 }
 
+// Tuning override, read at each call: SSDNN_KX = 1 runs 2:4 SM-pair tiles with
+// stages of one 128-byte K step instead of two.
+int kx_override() {
+  const char* e = getenv("SSDNN_KX");
+  return e ? atoi(e) : 0;
+}
+
 template <int DT>
 cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   constexpr int EB = Elem<DT>::bytes;
   if (mode == 0 || mode == 1) {
     const bool sparse = mode == 1;
     TileChoice c = choose_tile(sparse, EB, a.M, a.N);
+    // large 16-bit 2:4 problems: SM pairs with two-step stages (measured ahead of
+    // the 256 x 192 single-CTA tiles the fill model picks there)
+    if (sparse && EB == 2 && c.mt == 2 && c.bn == 192) c = TileChoice{1, 256, true};
     if (const int ov = tile_override()) c = TileChoice{ov / 1000 == 9 ? 1 : ov / 1000, ov % 1000, ov / 1000 == 9};
     if (c.pair && sparse) {
       // the metadata tensor map addresses 128-row blocks by an int32 row coordinate
@@ -1077,8 +1107,12 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
     }
     if (c.pair) {
       if (c.bn != 256) return cudaErrorInvalidValue;
-      return sparse ? run<DT, true, false, 256, 1, 1, 128, true>(a, s, err)
-                    : run<DT, false, false, 256, 1, 1, 128, true>(a, s, err);
+      // 2:4: stages of two 128-byte K steps halve the ring's turnovers (each stage
+      // costs a fixed share of the operand stream, whatever its size)
+      if (sparse)
+        return kx_override() == 1 ? run<DT, true, false, 256, 1, 1, 128, true>(a, s, err)
+                                  : run<DT, true, false, 256, 1, 1, 128, true, false, false, 2>(a, s, err);
+      return run<DT, false, false, 256, 1, 1, 128, true>(a, s, err);
     }
     if (c.mt == 2) {
       if (!sparse && c.bn == 256) return run<DT, false, false, 256, 1, 2>(a, s, err);

@@ -190,7 +190,7 @@ FORCED_SHAPES = [(300, 264, 520), (2000, 8192, 256)]
 
 def _forced_tiles(dt, sparse):
     tiles = ["1128", "1256", "9256"] + (["1064"] if dt != "e4m3" else [])
-    return tiles + (["2192"] if sparse else ["2256"])
+    return tiles + (["2192", "9256k2"] if sparse else ["2256"])
 
 
 @pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
@@ -213,7 +213,9 @@ def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
         B = oracle.gemm.bound(W, X, dt, alpha)
     Xd = dev_padded(X, dt)
     for tile in _forced_tiles(dt, sparse):
-        monkeypatch.setenv("SSDNN_TILE", tile)
+        # "k2": SM-pair stages of two 128-byte K steps
+        monkeypatch.setenv("SSDNN_TILE", tile.split("k")[0])
+        monkeypatch.setenv("SSDNN_KX", "2" if tile.endswith("k2") else "1")
         Y, buf = guarded_output(M, N, torch.bfloat16 if out_dt == "bf16" else torch.float16)
         if sparse:
             ss.sp24_gemm(f, Xd, alpha=alpha, out=Y)
@@ -226,14 +228,15 @@ def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "e4m3"])
-@pytest.mark.parametrize("tile", [None, "1128", "9256"])
+@pytest.mark.parametrize("tile", [None, "1128", "9256", "9256k2"])
 def test_sp24_gemm_host_direct_output(dt, tile, monkeypatch):
     """Y_dev None: the epilogue stores straight into page-locked host memory. The
     result is bit-identical to the same tiles' device output, and nothing outside
     the M x N view of the pinned buffer is written."""
     ss = lib()
     if tile:
-        monkeypatch.setenv("SSDNN_TILE", tile)
+        monkeypatch.setenv("SSDNN_TILE", tile.split("k")[0])
+        monkeypatch.setenv("SSDNN_KX", "2" if tile.endswith("k2") else "1")
     M, N, K = 1000, 264, 512
     W = rand_bits(811, (M, K), dt, 0.5)
     X = rand_bits(812, (K, N), dt, 1.0)
