@@ -128,8 +128,12 @@ struct Cfg {
   // into one of two 2 KB shared-memory buffers and a TMA store writes it out, so
   // the accumulator is drained without waiting on global stores.
   static constexpr bool STAGED = !GATHER && !CONV;
-  static constexpr int STAGING_BYTES = STAGED ? EPI_WARPS * 4096 : 0;
-  static constexpr int STAGES_RAW = (220 * 1024 - STAGING_BYTES) / STAGE_BYTES;
+  // two 2 KB buffers per epilogue warp; one for the 52 KB two-step stages, whose ring
+  // then gets a fourth stage within the 227 KB a CTA may hold
+  static constexpr int STAGING_BUFS = KX == 2 ? 1 : 2;
+  static constexpr int STAGING_BYTES = STAGED ? EPI_WARPS * 2048 * STAGING_BUFS : 0;
+  static constexpr int SMEM_BUDGET = KX == 2 ? 227 * 1024 - 1024 - 256 : 220 * 1024;
+  static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int MMA_K = (SPARSE ? 64 : 32) / EB;      // dense K per instruction
   static constexpr int MMAS = BK / MMA_K;                    // instructions per stage
@@ -153,6 +157,7 @@ struct Cfg {
                                                BN, false, !CONV);
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(STAGES >= 2, "the shared-memory ring needs two stages");
+  static_assert(SMEM_BYTES <= 227 * 1024, "more shared memory than a CTA may hold");
   static_assert(CONV || B_BOXES * B_BOX_COLS == BN_CTA, "BN must be a multiple of the B box width");
   static_assert(BN % 32 == 0, "the epilogue drains 32-column chunks");
   static_assert(!PAIR || (MT == 1 && CS == 1 && !GATHER), "SM pairs: one 128-row sub-tile per CTA");
@@ -761,9 +766,16 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
             if (row_ok) store_packed_row32(yrow, n0, p.N, p.out_dt, w, pol_y);
             continue;
           }
-          uint8_t* buf = staging + (warp - C::EPI_WARP0) * 4096 + (chunk_seq & 1) * 2048;
+          uint8_t* buf = staging + (warp - C::EPI_WARP0) * (2048 * C::STAGING_BUFS) +
+                         (C::STAGING_BUFS == 2 ? (chunk_seq & 1) * 2048 : 0);
           ++chunk_seq;
-          if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last used this buffer has read it
+          // the store that last used this buffer has read it
+          if (lane == 0) {
+            if constexpr (C::STAGING_BUFS == 2)
+              ptx::bulk_wait_read<1>();
+            else
+              ptx::bulk_wait_read<0>();
+          }
           __syncwarp();
           stage_packed_row32(buf, lane, p.out_dt, w);
           ptx::fence_proxy_async_smem();
