@@ -1,5 +1,5 @@
 // Inline-PTX wrappers for the Blackwell (sm_103a) instructions the kernels use:
-// mbarrier, TMA (tiled, gather4, 1-D bulk), and tcgen05 (TMEM alloc, MMA,
+// mbarrier, TMA (tiled, 1-D bulk), and tcgen05 (TMEM alloc, MMA,
 // sparse MMA, smem->TMEM copy, TMEM loads, commit, fences).
 #pragma once
 #include <cstdint>
@@ -81,19 +81,6 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorM
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
-// Four rows r0..r3 of a 2-D tensor (box one row high) land in four consecutive
-// box-rows of dst.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t col,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "l"(policy)
       : "memory");
 }
 
