@@ -171,6 +171,25 @@ def timed_steps(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> lis
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def host_link_rates(X_dev, X_host, Y_dev, Y_host, stream) -> dict:
+    """Copy-engine rates of the host link for this step's buffers (pinned host X in,
+    device Y out), GB/s, best of three: the floor the end-to-end number runs against."""
+    out = {}
+    for key, dst, src in (("h2d_gbs", X_dev, X_host), ("d2h_gbs", Y_host, Y_dev)):
+        nbytes = src.numel() * src.element_size()
+        ts = []
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        out[key] = round(nbytes / min(ts) / 1e6, 1)
+    return out
+
+
 def mma_microbench(ss, stream) -> dict:
     """Dense and 2:4-sparse tcgen05.mma rates with operands on chip (one CTA per
     SM), in dense-equivalent TFLOP/s, for the instruction shapes the GEMMs use."""
@@ -301,6 +320,10 @@ def run_gpu(args) -> None:
         e2e_ms[key] = statistics.mean(timed_steps(fn, max(3, args.steps // 2), 2, flush, stream))
     e2e_best = min(e2e_ms, key=e2e_ms.get)
     e2e_value = ws * eff_flops / (e2e_ms[e2e_best] * 1e-3) / 1e12
+    link = host_link_rates(Xd, X_host, Y, Y_host, stream)
+    x_bytes, y_bytes = Xd.numel() * Xd.element_size(), Y.numel() * Y.element_size()
+    # the end-to-end floor: X in and Y out over the host link, the GEMM fully hidden
+    link_ms = x_bytes / link["h2d_gbs"] / 1e6 + y_bytes / link["d2h_gbs"] / 1e6
 
     rows = {}
     mma = None
@@ -330,8 +353,9 @@ def run_gpu(args) -> None:
                                       f"{pk['bf16_tflops']}"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "path": e2e_paths[e2e_best][1],
                     "ms_per_step": {k: round(v, 4) for k, v in e2e_ms.items()},
-                    "h2d_bytes_per_step": int(Xd.numel() * Xd.element_size()),
-                    "d2h_bytes_per_step": int(Y.numel() * Y.element_size())},
+                    "h2d_bytes_per_step": int(x_bytes), "d2h_bytes_per_step": int(y_bytes),
+                    "host_link_gbs": link, "link_bound_ms": round(link_ms, 4),
+                    "frac_of_link_bound": round(link_ms / e2e_ms[e2e_best], 4)},
             "mma_microbench_dense_equivalent_tflops": mma,
             "gpu_launches": args.steps,
             "clocks": clocks,
