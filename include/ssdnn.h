@@ -313,6 +313,28 @@ int bw_gemm_ep(int dt, int out_dt, int64_t M, int64_t N, int64_t K, const int32_
                const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
                void* stream);
 
+/* ------------------------------------------------------ tile variants ----
+ * sp24_gemm_ep / dense_gemm_ep with an explicit tile variant instead of the one
+ * the library picks from the shape (for tuning and for tests that must run
+ * every variant; the results are identical up to fp32 summation order):
+ *   0      chosen by shape (the plain calls)
+ *   1064   128 x 64 tiles, one CTA (fp16/bf16 only)
+ *   1128   128 x 128 tiles, one CTA
+ *   1256   128 x 256 tiles, one CTA
+ *   2192   256 x 192 tiles, one CTA with two M = 128 instructions (2:4 only)
+ *   2256   256 x 256 tiles, one CTA with two M = 128 instructions (dense only)
+ *   9256   256 x 256 tiles on an SM pair (cta_group::2), one 128-byte K step per stage
+ *   19256  the same with two K steps per stage (2:4 only)
+ * Any other value, or one the operand type does not have: SSDNN_ERR_UNSUPPORTED,
+ * before any work is enqueued. The pages have no counterpart: this selects among
+ * implementations of the same product. */
+int sp24_gemm_variant(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+                      const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                      const ssdnn_epilogue* ep, int variant, void* stream);
+int dense_gemm_variant(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
+                       const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+                       int variant, void* stream);
+
 /* ------------------------------------------------- allocation-free variant ----
  * tw_prune_compress_noalloc: tw_prune_compress for callers that cannot allocate
  * device memory. (The pages have no counterpart: this is a deployment aid.)
@@ -329,9 +351,14 @@ int bw_gemm_ep(int dt, int out_dt, int64_t M, int64_t N, int64_t K, const int32_
  * Limits: nt = ceil(M/128) <= SSDNN_NOALLOC_MAX_TILES and nt * K <=
  * SSDNN_NOALLOC_MAX_SCORES; beyond them it returns SSDNN_ERR_UNSUPPORTED and does
  * nothing.
- * Set-up: the first call on each device looks up the device address of that
- * array (with the device current); make that first call before any stream
- * capture.
+ * Set-up: every call looks up the device address of that array with the
+ * device current (a lookup that allocates nothing). The first call on a device
+ * may also be the first use of the library's kernels there, and with lazy
+ * module loading (CUDA_MODULE_LOADING=LAZY, the default) the CUDA runtime then
+ * loads the module, which takes device memory once. Callers that may not
+ * allocate at all should make one call during their set-up, before any stream
+ * capture; later calls allocate nothing. A device reset invalidates nothing the
+ * library keeps: the address is looked up again on the next call.
  * Sharing: all calls on a device share the one array, which keeps the last call's
  * scores (every call overwrites the part it reads, so nothing needs clearing).
  * Calls whose work overlaps on the GPU (different streams without ordering) race

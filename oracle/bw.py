@@ -27,6 +27,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import codecs, tw
+from . import gemm as products
 
 T = 128
 BW = 64
@@ -107,5 +108,5 @@ def gemm(form: dict, keep_blocks: np.ndarray, X: np.ndarray, dt: str, out_dt: st
         cols = form["col_indices"][BW * off[t]:BW * off[t + 1]]
         Wt = codecs.decode(unpack_tile(form, keep_blocks, t), dt)
         Yf[t * T:(t + 1) * T] = alpha * (Wt @ Xd[cols])
-        B[t * T:(t + 1) * T] = abs(alpha) * (np.abs(Wt) @ np.abs(Xd[cols]))
+        B[t * T:(t + 1) * T] = products.bound_decoded(Wt, Xd[cols], alpha)
     return codecs.encode(Yf[:M], out_dt), B[:M]

@@ -23,6 +23,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import codecs
+from . import gemm as products
 
 _MAG = {"f16": 0x7FFF, "bf16": 0x7FFF, "e4m3": 0x7F}
 
@@ -70,5 +71,5 @@ def spmm(form: dict, M: int, K: int, X: np.ndarray, dt: str, out_dt: str, alpha:
         w = codecs.decode(vals_all[i], dt)
         xk = Xd[cols_all[i]]
         Y[j] = alpha * (w @ xk)
-        B[j] = abs(alpha) * (np.abs(w) @ np.abs(xk))
+        B[j] = products.bound_decoded(w, xk, alpha)
     return codecs.encode(Y, out_dt), B

@@ -26,11 +26,17 @@ def dense_product(W: np.ndarray, X: np.ndarray, dt: str, alpha: float = 1.0,
     return alpha * (Wd @ Xd)
 
 
+def bound_decoded(Wd: np.ndarray, Xd: np.ndarray, alpha: float = 1.0) -> np.ndarray:
+    """B_ij = |alpha| * sum_k |w_ik| |x_kj| in fp64 from decoded values: the scale of
+    the elementwise tolerance |Y - Y_ref| <= rel * B. Every product form of the
+    oracle (2:4, dense, tile-wise, block-wise, element-wise, convolution) takes its
+    bound from here, over the weights it actually multiplies (the pruned ones)."""
+    return abs(alpha) * (np.abs(Wd) @ np.abs(Xd))
+
+
 def bound(W: np.ndarray, X: np.ndarray, dt: str, alpha: float = 1.0, rows=None) -> np.ndarray:
-    """|alpha| * sum_k |w_ik| |x_kj| in fp64."""
-    Wd = np.abs(codecs.decode(W if rows is None else W[rows], dt))
-    Xd = np.abs(codecs.decode(X, dt))
-    return abs(alpha) * (Wd @ Xd)
+    """|alpha| * sum_k |w_ik| |x_kj| in fp64 (W and X as stored bits)."""
+    return bound_decoded(codecs.decode(W if rows is None else W[rows], dt), codecs.decode(X, dt), alpha)
 
 
 def gemm_dense(W: np.ndarray, X: np.ndarray, dt: str, out_dt: str, alpha: float = 1.0,

@@ -34,6 +34,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import codecs, sp24
+from . import gemm as products
 
 T = 128
 U = 64
@@ -178,5 +179,5 @@ def gemm(form: dict, keep: np.ndarray, X: np.ndarray, dt: str, out_dt: str, M: i
         Wt = codecs.decode(unpack_tile(form, keep, t, tvw, dt), dt)
         Xt = Xd[idx]
         Yf[t * T:(t + 1) * T] = alpha * (Wt @ Xt)
-        B[t * T:(t + 1) * T] = abs(alpha) * (np.abs(Wt) @ np.abs(Xt))
+        B[t * T:(t + 1) * T] = products.bound_decoded(Wt, Xt, alpha)
     return codecs.encode(Yf[:M], out_dt), B[:M]

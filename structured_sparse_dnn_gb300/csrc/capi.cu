@@ -199,9 +199,10 @@ int build_bw_tables(int64_t M, int64_t K, const int32_t* keep_blocks, BwTables* 
 }  // namespace
 int sp24_gemm_impl(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
                    const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
-                   const ssdnn_epilogue* ep, bool f8_out_ok, void* stream) {
+                   const ssdnn_epilogue* ep, bool f8_out_ok, void* stream, int variant = 0) {
   if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
   const int eb = elem_bytes(in_dt);
+  if (!gemm_variant_ok(variant, true, eb)) return SSDNN_ERR_UNSUPPORTED;
   int st = check_gemm_io(out_dt, f8_out_ok, M, N, K, X, ldx, eb, Y, ldy);
   if (st == SSDNN_OK) st = check_epilogue(ep);
   if (st != SSDNN_OK || M == 0 || N == 0) return st;
@@ -224,15 +225,17 @@ int sp24_gemm_impl(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const
   a.Y = Y;
   a.ldy = ldy;
   a.alpha = alpha;
+  a.variant = variant;
   set_epilogue(a, ep);
   return from_cuda(launch_gemm(1, a, s, error_word()));
 }
 
 int dense_gemm_impl(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
                     const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
-                    bool f8_out_ok, void* stream) {
+                    bool f8_out_ok, void* stream, int variant = 0) {
   if (!valid_dt(in_dt)) return SSDNN_ERR_INVALID_ARG;
   const int eb = elem_bytes(in_dt);
+  if (!gemm_variant_ok(variant, false, eb)) return SSDNN_ERR_UNSUPPORTED;
   int st = check_gemm_io(out_dt, f8_out_ok, M, N, K, X, ldx, eb, Y, ldy);
   if (st == SSDNN_OK) st = check_epilogue(ep);
   if (st != SSDNN_OK || M == 0 || N == 0) return st;
@@ -253,6 +256,7 @@ int dense_gemm_impl(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, cons
   a.Y = Y;
   a.ldy = ldy;
   a.alpha = alpha;
+  a.variant = variant;
   set_epilogue(a, ep);
   return from_cuda(launch_gemm(0, a, s, error_word()));
 }
@@ -491,6 +495,18 @@ int dense_gemm_ep(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const 
                   const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
                   void* stream) {
   return dense_gemm_impl(in_dt, out_dt, M, N, K, W, ldw, X, ldx, Y, ldy, alpha, ep, true, stream);
+}
+
+int sp24_gemm_variant(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* values,
+                      const uint8_t* meta_hw, const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha,
+                      const ssdnn_epilogue* ep, int variant, void* stream) {
+  return sp24_gemm_impl(in_dt, out_dt, M, N, K, values, meta_hw, X, ldx, Y, ldy, alpha, ep, true, stream, variant);
+}
+
+int dense_gemm_variant(int in_dt, int out_dt, int64_t M, int64_t N, int64_t K, const void* W, int64_t ldw,
+                       const void* X, int64_t ldx, void* Y, int64_t ldy, float alpha, const ssdnn_epilogue* ep,
+                       int variant, void* stream) {
+  return dense_gemm_impl(in_dt, out_dt, M, N, K, W, ldw, X, ldx, Y, ldy, alpha, ep, true, stream, variant);
 }
 
 int tw_sizes(int dt, int tvw, int64_t M, int64_t K, const int32_t* keep_counts_host, size_t* packed_bytes,

@@ -39,7 +39,6 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -51,7 +50,7 @@ struct Params {
   int32_t M, N;
   int32_t MB, NB;           // BM-row blocks (BM = 128 MT), BN-column blocks
   int32_t MB128;            // 128-row blocks (the metadata's row blocks)
-  int32_t MG;               // groups of CS consecutive BM-row blocks (one group per cluster pass)
+  int32_t MG;               // groups of CLUSTER consecutive BM-row blocks (one group per cluster pass)
   int32_t GR;               // rasterisation: M groups per band; work sweeps a band's N blocks
   int32_t num_units;        // work items: (M group, N block) pairs, or (schedule entry, N block)
   int32_t nk;               // k stages per unit (dense / sp24)
@@ -78,7 +77,7 @@ struct Params {
   int32_t y_direct;                             // Y is page-locked host memory: plain stores, no TMA
 };
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW = 128, bool PAIR = false,
+template <int DT, bool SPARSE, bool GATHER, int BN, int MT, int BROW = 128, bool PAIR = false,
           bool BLOCKW = false, bool CONV = false, int KX = 1>
 struct Cfg {
   // CONV: 3x3 convolution as an implicit GEMM -- the B operand of a K stage is one
@@ -90,11 +89,10 @@ struct Cfg {
   static constexpr bool BLOCKWISE = BLOCKW;
   static constexpr bool SCHEDULED = GATHER || BLOCKW;         // work follows the tile schedule
   // PAIR: the two CTAs of a cluster form an SM pair running M = 256 MMAs (each CTA
-  // holds 128 rows of A, BN/2 columns of B and its 128 accumulator rows); else
-  // CS > 1 CTAs of a cluster share one X panel by multicast.
+  // holds 128 rows of A, BN/2 columns of B and its 128 accumulator rows); every
+  // CTA loads its own operands (no multicast).
   static constexpr bool PAIRED = PAIR;
-  static constexpr int CLUSTER = PAIR ? 2 : CS;             // CTAs per cluster
-  static constexpr bool MCAST = !PAIR && CS > 1;
+  static constexpr int CLUSTER = PAIR ? 2 : 1;              // CTAs per cluster
   static constexpr int BN_CTA = PAIR ? BN / 2 : BN;         // B columns held by this CTA
   static constexpr int SUB = MT;                            // 128-row sub-tiles per CTA tile
   static constexpr int BM = 128 * MT;
@@ -160,16 +158,13 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "more shared memory than a CTA may hold");
   static_assert(CONV || B_BOXES * B_BOX_COLS == BN_CTA, "BN must be a multiple of the B box width");
   static_assert(BN % 32 == 0, "the epilogue drains 32-column chunks");
-  static_assert(!PAIR || (MT == 1 && CS == 1 && !GATHER), "SM pairs: one 128-row sub-tile per CTA");
-  static_assert(!BLOCKW || (!SPARSE && !GATHER && !PAIR && MT == 1 && CS == 1), "block-wise: dense 128-row tiles");
-  static_assert(!CONV || (!GATHER && !PAIR && !BLOCKW && MT == 1 && CS == 1 && Elem<DT>::bytes == 2),
+  static_assert(!PAIR || (MT == 1 && !GATHER), "SM pairs: one 128-row sub-tile per CTA");
+  static_assert(!BLOCKW || (!SPARSE && !GATHER && !PAIR && MT == 1), "block-wise: dense 128-row tiles");
+  static_assert(!CONV || (!GATHER && !PAIR && !BLOCKW && MT == 1 && Elem<DT>::bytes == 2),
                 "convolution: 16-bit, 128-row tiles");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
   static_assert(KX == 1 || (KX == 2 && SPARSE && PAIR), "double K stages: 2:4 on SM pairs");
-  static_assert(MT == 1 || (CS == 1 && !GATHER), "256-row tiles: no cluster, no gather");
-  static_assert(CS == 1 || !GATHER, "gathered B rows differ per tile: no multicast");
-  static constexpr int B_SLICE_ROWS = BK / (MCAST ? CS : 1); // rows of each B box this CTA loads
-  static_assert(B_SLICE_ROWS % 8 == 0, "B slices must keep whole 8-row swizzle atoms");
+  static_assert(MT == 1 || !GATHER, "256-row tiles: no gather");
 };
 
 // N width of one output tile (both CTAs of a pair write all of it for their rows).
@@ -338,16 +333,11 @@ __device__ __forceinline__ void stage_packed_row32(uint8_t* buf, uint32_t lane, 
         make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT, int BROW, bool PAIR, bool BLOCKW, bool CONV,
-          int KX>
-__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>::THREADS, 1)
+template <int DT, bool SPARSE, bool GATHER, int BN, int MT, int BROW, bool PAIR, bool BLOCKW, bool CONV, int KX>
+__global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BLOCKW, CONV, KX>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>;
-  // Multicast clusters (CS CTAs along M) share each X panel: CTA rank r loads rows
-  // [r BK/CS, (r+1) BK/CS) of every B box of a stage and multicasts them to the
-  // whole cluster, so a stage is complete only when all CS slices have landed and
-  // can be refilled only when all CS MMA issuers have released it.
+  using C = Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BLOCKW, CONV, KX>;
   // SM pairs (PAIR): both CTAs load their own A rows, metadata and B columns, all
   // counted on the even CTA's full barrier; the even CTA's MMA thread issues the
   // M = 256 MMAs and its commits release both CTAs' stages and accumulators; the odd
@@ -390,7 +380,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(&full[s], 1 + C::GATHER_THREADS);
-      ptx::mbar_init(&empty[s], C::MCAST ? CS : 1);
+      ptx::mbar_init(&empty[s], 1);
       if constexpr (KX == 2) ptx::mbar_init(&full_b[s], 1);
     }
     for (int a = 0; a < C::NACC; ++a) {
@@ -417,7 +407,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
   }
   ptx::tc_fence_before();
   if constexpr (CL > 1)
-    ptx::cluster_sync();  // peers' barriers are initialised before any multicast reaches them
+    ptx::cluster_sync();  // the peer's barriers are initialised before any arrival reaches them
   else
     __syncthreads();
   ptx::tc_fence_after();
@@ -479,20 +469,12 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
             const int32_t r = tap / 3, sx = tap - 3 * r;
             ptx::tma_load_4d(sB, &tmB, &full[stage], c0, sx - 1, ui.h0 + r - 1, ui.img, pol_b);
           } else if constexpr (!GATHER) {
-            if constexpr (!C::MCAST) {
-              // block-wise: the X panel of the kb-th kept block of this tile
-              const int32_t krow = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) * C::BK : kb * C::BK;
+            // block-wise: the X panel of the kb-th kept block of this tile
+            const int32_t krow = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) * C::BK : kb * C::BK;
 #pragma unroll
-              for (int bx = 0; bx < C::B_BOXES; ++bx)
-                ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS, krow,
-                                 pol_b);
-            } else {
-              const int32_t r0 = static_cast<int32_t>(crank) * C::B_SLICE_ROWS;
-#pragma unroll
-              for (int bx = 0; bx < C::B_BOXES; ++bx)
-                ptx::tma_load_2d_multicast(sB + bx * C::B_BOX_BYTES + r0 * C::B_ROW, &tmB, &full[stage],
-                                           ui.n0 + bx * C::B_BOX_COLS, kb * C::BK + r0, kMask, pol_b);
-            }
+            for (int bx = 0; bx < C::B_BOXES; ++bx)
+              ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS, krow,
+                               pol_b);
           }
           }
         }
@@ -602,8 +584,6 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
           }
           if constexpr (PAIR)
             ptx::mma_commit_pair_multicast(&empty[stage], kMask);
-          else if constexpr (C::MCAST)
-            ptx::mma_commit_multicast(&empty[stage], kMask);
           else
             ptx::mma_commit(&empty[stage]);
         }
@@ -811,7 +791,6 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR
     else
       ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if constexpr (C::MCAST) ptx::cluster_sync();  // no CTA leaves while a peer may still signal it
 }
 
 // ------------------------------------------------------------------ host side
@@ -870,10 +849,10 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int DT, bool SPARSE, bool GATHER, int BN, int CS, int MT = 1, int BROW = 128, bool PAIR = false,
+template <int DT, bool SPARSE, bool GATHER, int BN, int MT = 1, int BROW = 128, bool PAIR = false,
           bool BLOCKW = false, bool CONV = false, int KX = 1>
 cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  using C = Cfg<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>;
+  using C = Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BLOCKW, CONV, KX>;
   const int eb = C::EB;
   CUtensorMap tA, tB, tM;
   bool ok;
@@ -893,7 +872,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   } else if constexpr (BLOCKW) {
     // the packed kept blocks seen as (packed_rows x 64); X as for the dense GEMM
     ok = make_map(&tA, a.A, eb, 64, a.packed_rows, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::B_SLICE_ROWS,
+    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::BK,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   } else if constexpr (!GATHER) {
     if constexpr (SPARSE && KX == 2)
@@ -904,7 +883,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
                     CU_TENSOR_MAP_SWIZZLE_64B);
     else
       ok = make_map(&tA, a.A, eb, a.K, a.M, a.lda * eb, 128 / eb, C::BM, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::B_SLICE_ROWS,
+    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::BK,
                         BROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
     // packed operand seen as (packed_rows x 64) dense or (packed_rows x 32) values
@@ -982,10 +961,6 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.bias = a.bias;
   p.y_scale = a.y_scale;
   p.nstages = C::STAGES;
-  if (const char* e = getenv("SSDNN_STAGES")) {  // tuning: a shorter ring than shared memory allows
-    const int v = atoi(e);
-    if (v >= 2 && v < C::STAGES) p.nstages = v;
-  }
   p.alpha = a.alpha;
   p.meta_hw = a.meta_hw;
   p.schedule = a.schedule;
@@ -999,7 +974,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.y_direct = y_host ? 1 : 0;
   if (p.num_units == 0) return cudaSuccess;
 
-  auto kern = k_gemm<DT, SPARSE, GATHER, BN, CS, MT, BROW, PAIR, BLOCKW, CONV, KX>;
+  auto kern = k_gemm<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BLOCKW, CONV, KX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   constexpr int CL = C::CLUSTER;
@@ -1030,27 +1005,6 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
     return cudaLaunchKernelEx(&cfg, kern, tA, tB, tM, tY, p);
   }
-}
-
-int cluster_override() {
-  static int v = [] {
-    const char* e = getenv("SSDNN_CLUSTER");
-    return e ? atoi(e) : 0;
-  }();
-  return v;
-}
-
-template <int DT, bool SPARSE, int BN>
-cudaError_t run_clustered(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
-  // Clusters of CTAs on consecutive 128-row blocks of one N block share its X
-  // panel by multicast (opt-in: SSDNN_CLUSTER=2 or 4; measured no faster than
-  // one CTA per panel on the LLM FFN shapes, where the per-SM fill rate, not L2,
-  // limits the kernel).
-  const int64_t MB = ceil_div(a.M, 128);
-  const int ov = cluster_override();
-  if (ov == 4 && MB >= 4) return run<DT, SPARSE, false, BN, 4>(a, s, err);
-  if (ov == 2 && MB >= 2) return run<DT, SPARSE, false, BN, 2>(a, s, err);
-  return run<DT, SPARSE, false, BN, 1>(a, s, err);
 }
 
 // Tile choice by a fill-rate model: a CTA's time is its stage count times the
@@ -1088,20 +1042,6 @@ TileChoice choose_tile(bool sparse, int eb, int64_t M, int64_t N) {
   return best;
 }
 
-// Tuning override, read at each call: SSDNN_TILE = MT * 1000 + BN (e.g. 2192), or
-// 9000 + BN for an SM-pair tile (e.g. 9256).
-int tile_override() {
-  const char* e = getenv("SSDNN_TILE");
-  return e ? atoi(e) : 0;
-}
-
-// Tuning override, read at each call: SSDNN_KX = 1 runs 2:4 SM-pair tiles with
-// stages of one 128-byte K step instead of two.
-int kx_override() {
-  const char* e = getenv("SSDNN_KX");
-  return e ? atoi(e) : 0;
-}
-
 template <int DT>
 cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   constexpr int EB = Elem<DT>::bytes;
@@ -1111,7 +1051,12 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
     // large 16-bit 2:4 problems: SM pairs with two-step stages (measured ahead of
     // the 256 x 192 single-CTA tiles the fill model picks there)
     if (sparse && EB == 2 && c.mt == 2 && c.bn == 192) c = TileChoice{1, 256, true};
-    if (const int ov = tile_override()) c = TileChoice{ov / 1000 == 9 ? 1 : ov / 1000, ov % 1000, ov / 1000 == 9};
+    int kx = 2;  // 2:4 SM-pair tiles: stages of two 128-byte K steps
+    if (a.variant) {  // an explicit tile variant (validated by the caller)
+      const int v = a.variant % 10000;
+      c = TileChoice{v / 1000 == 9 ? 1 : v / 1000, v % 1000, v / 1000 == 9};
+      kx = a.variant >= 10000 ? 2 : 1;
+    }
     if (c.pair && sparse) {
       // the metadata tensor map addresses 128-row blocks by an int32 row coordinate
       const int64_t meta_rows = ceil_div(a.M, 128) * ceil_div(a.K, 128 / EB) * 16;
@@ -1122,28 +1067,28 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
       // 2:4: stages of two 128-byte K steps halve the ring's turnovers (each stage
       // costs a fixed share of the operand stream, whatever its size)
       if (sparse)
-        return kx_override() == 1 ? run<DT, true, false, 256, 1, 1, 128, true>(a, s, err)
-                                  : run<DT, true, false, 256, 1, 1, 128, true, false, false, 2>(a, s, err);
-      return run<DT, false, false, 256, 1, 1, 128, true>(a, s, err);
+        return kx == 1 ? run<DT, true, false, 256, 1, 128, true>(a, s, err)
+                                  : run<DT, true, false, 256, 1, 128, true, false, false, 2>(a, s, err);
+      return run<DT, false, false, 256, 1, 128, true>(a, s, err);
     }
     if (c.mt == 2) {
-      if (!sparse && c.bn == 256) return run<DT, false, false, 256, 1, 2>(a, s, err);
+      if (!sparse && c.bn == 256) return run<DT, false, false, 256, 2>(a, s, err);
       if (sparse && EB == 2 && c.bn == 192) {
-        if constexpr (EB == 2) return run<DT, true, false, 192, 1, 2>(a, s, err);
+        if constexpr (EB == 2) return run<DT, true, false, 192, 2>(a, s, err);
       }
       if (sparse && EB == 1 && c.bn == 192) {
-        if constexpr (EB == 1) return run<DT, true, false, 192, 1, 2, 64>(a, s, err);
+        if constexpr (EB == 1) return run<DT, true, false, 192, 2, 64>(a, s, err);
       }
       return cudaErrorInvalidValue;
     }
     if (c.bn == 64) {
       if constexpr (EB == 2)
-        return sparse ? run<DT, true, false, 64, 1>(a, s, err) : run<DT, false, false, 64, 1>(a, s, err);
+        return sparse ? run<DT, true, false, 64>(a, s, err) : run<DT, false, false, 64>(a, s, err);
       return cudaErrorInvalidValue;
     }
     if (c.bn == 128)
-      return sparse ? run_clustered<DT, true, 128>(a, s, err) : run_clustered<DT, false, 128>(a, s, err);
-    return sparse ? run_clustered<DT, true, 256>(a, s, err) : run_clustered<DT, false, 256>(a, s, err);
+      return sparse ? run<DT, true, false, 128>(a, s, err) : run<DT, false, false, 128>(a, s, err);
+    return sparse ? run<DT, true, false, 256>(a, s, err) : run<DT, false, false, 256>(a, s, err);
   }
   if (mode == 5 || mode == 6) {
     // 3x3 convolution: N tiles of whole image rows, 224 columns (128 when that leaves
@@ -1152,22 +1097,21 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
       const int64_t units224 = ceil_div(a.M, 128) * a.conv_nb * ceil_div(a.conv_h, 224 / a.conv_w);
       const bool narrow_c = a.conv_w <= 128 && units224 < 2 * sm_count();
       if (mode == 5)
-        return narrow_c ? run<DT, true, false, 128, 1, 1, 128, false, false, true>(a, s, err)
-                        : run<DT, true, false, 224, 1, 1, 128, false, false, true>(a, s, err);
-      return narrow_c ? run<DT, false, false, 128, 1, 1, 128, false, false, true>(a, s, err)
-                      : run<DT, false, false, 224, 1, 1, 128, false, false, true>(a, s, err);
+        return narrow_c ? run<DT, true, false, 128, 1, 128, false, false, true>(a, s, err)
+                        : run<DT, true, false, 224, 1, 128, false, false, true>(a, s, err);
+      return narrow_c ? run<DT, false, false, 128, 1, 128, false, false, true>(a, s, err)
+                      : run<DT, false, false, 224, 1, 128, false, false, true>(a, s, err);
     }
     return cudaErrorInvalidValue;
   }
   // tile-wise and block-wise: 128-row tiles follow the pattern's tiles
-  bool narrow = a.N <= 128 || a.nt * ceil_div(a.N, 256) < 2 * sm_count();
-  if (const char* e = getenv("SSDNN_GATHER_BN")) narrow = atoi(e) == 128;  // tuning
+  const bool narrow = a.N <= 128 || a.nt * ceil_div(a.N, 256) < 2 * sm_count();
   if constexpr (DT != 2) {
-    if (mode == 2) return narrow ? run<DT, false, true, 128, 1>(a, s, err) : run<DT, false, true, 256, 1>(a, s, err);
-    if (mode == 3) return narrow ? run<DT, true, true, 128, 1>(a, s, err) : run<DT, true, true, 256, 1>(a, s, err);
+    if (mode == 2) return narrow ? run<DT, false, true, 128>(a, s, err) : run<DT, false, true, 256>(a, s, err);
+    if (mode == 3) return narrow ? run<DT, true, true, 128>(a, s, err) : run<DT, true, true, 256>(a, s, err);
     if (mode == 4)
-      return narrow ? run<DT, false, false, 128, 1, 1, 128, false, true>(a, s, err)
-                    : run<DT, false, false, 256, 1, 1, 128, false, true>(a, s, err);
+      return narrow ? run<DT, false, false, 128, 1, 128, false, true>(a, s, err)
+                    : run<DT, false, false, 256, 1, 128, false, true>(a, s, err);
   }
   return cudaErrorInvalidValue;
 }
@@ -1202,6 +1146,16 @@ cudaError_t launch_fill_epilogue(void* Y, int64_t ldy, int64_t M, int64_t N, int
                   static_cast<unsigned>(std::min<int64_t>(M, 65535)));
   k_fill_epilogue<<<grid, 256, 0, s>>>(static_cast<uint8_t*>(Y), ldy, M, N, code, bias, act, y_scale);
   return cudaGetLastError();
+}
+
+bool gemm_variant_ok(int variant, bool sparse, int elem_bytes) {
+  switch (variant) {
+    case 0: case 1128: case 1256: case 9256: return true;
+    case 1064: return elem_bytes == 2;
+    case 2192: case 19256: return sparse;
+    case 2256: return !sparse;
+  }
+  return false;
 }
 
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err) {

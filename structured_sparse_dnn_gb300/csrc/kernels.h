@@ -33,7 +33,15 @@ struct GemmArgs {
   const float* bias = nullptr;
   int act = 0;          // 0 none, 1 ReLU, 2 GELU
   float y_scale = 1.0f;
+  // dense / 2:4 GEMM tile variant: 0 = chosen by shape; else one of kGemmVariants
+  int variant = 0;
 };
+
+// Explicit tile variants of the dense and 2:4 GEMMs (tuning and tests):
+// MT * 1000 + BN for single-CTA tiles of 128 MT rows x BN columns, 9256 for SM-pair
+// 256 x 256 tiles with one 128-byte K step per stage, 19256 for SM-pair tiles with
+// two K steps per stage (2:4 only).
+bool gemm_variant_ok(int variant, bool sparse, int elem_bytes);
 
 // mode: 0 dense, 1 sp24, 2 TW (dense packed + gather), 3 TVW (2:4 packed + gather),
 // 4 block-wise (dense packed blocks, X panels by TMA), 5 / 6 3x3 convolution with a

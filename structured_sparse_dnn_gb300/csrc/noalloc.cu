@@ -8,8 +8,6 @@
 // which travel as a kernel parameter. Everything else runs the same kernels.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/ssdnn.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -26,26 +24,15 @@ struct KeepCounts {
   int32_t L[kMaxTiles];
 };
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-float* g_scores_ptr[kMaxDevices] = {};
-
 // Device address of the scratch for the current device. The host-side symbol is
-// only a stand-in, so the address is looked up once per device with that device
-// current.
+// only a stand-in, so the address is looked up with that device current, on
+// every call: the lookup allocates nothing, and an address cached across calls
+// would go stale if the device were reset and the module loaded again.
 cudaError_t scratch_address(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scores);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scores_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scores);
-    if (e != cudaSuccess) return e;
-    g_scores_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scores_ptr[dev];
+  *out = static_cast<float*>(p);
   return cudaSuccess;
 }
 

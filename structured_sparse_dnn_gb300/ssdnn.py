@@ -75,6 +75,10 @@ _SIGS = {
                            _ptr, _ptr], C.c_int),
     "tvw_gemm": ([C.c_int, C.c_int, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _ptr,
                   _i64, _ptr], C.c_int),
+    "sp24_gemm_variant": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _i64, _ptr, _i64, C.c_float, _epp,
+                           C.c_int, _ptr], C.c_int),
+    "dense_gemm_variant": ([C.c_int, C.c_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, C.c_float, _epp,
+                            C.c_int, _ptr], C.c_int),
     "tw_prune_compress_noalloc": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr,
                                    _ptr, _ptr], C.c_int),
 }
@@ -189,8 +193,9 @@ def _epilogue(bias: torch.Tensor | None, act: str, y_scale: float, M: int):
 
 def sp24_gemm(form: Sp24, X: torch.Tensor, out_dtype: torch.dtype | None = None, alpha: float = 1.0,
               out: torch.Tensor | None = None, bias: torch.Tensor | None = None, act: str = "none",
-              y_scale: float = 1.0):
-    """Y = round(y_scale * act(alpha * decompress(form) . X + bias[:, None]))  (M x N)."""
+              y_scale: float = 1.0, variant: int = 0):
+    """Y = round(y_scale * act(alpha * decompress(form) . X + bias[:, None]))  (M x N).
+    variant != 0 forces a tile variant (sp24_gemm_variant)."""
     dt = _DT[X.dtype]
     assert dt == form.dt and X.shape[0] == form.K
     N = X.shape[1]
@@ -200,7 +205,10 @@ def sp24_gemm(form: Sp24, X: torch.Tensor, out_dtype: torch.dtype | None = None,
     ep = _epilogue(bias, act, y_scale, form.M)
     args = (dt, _DT[out.dtype], form.M, N, form.K, _p(form.values), _p(form.meta_hw), _p(X), X.stride(0), _p(out),
             out.stride(0), alpha)
-    if ep is None and out.dtype != torch.float8_e4m3fn:
+    if variant:
+        _check(lib.sp24_gemm_variant(*args, None if ep is None else C.byref(ep), variant, _stream(X.device)),
+               "sp24_gemm_variant")
+    elif ep is None and out.dtype != torch.float8_e4m3fn:
         _check(lib.sp24_gemm(*args, _stream(X.device)), "sp24_gemm")
     else:
         _check(lib.sp24_gemm_ep(*args, None if ep is None else C.byref(ep), _stream(X.device)), "sp24_gemm_ep")
@@ -228,8 +236,9 @@ def sp24_gemm_host(form: Sp24, X_host: torch.Tensor, Y_host: torch.Tensor, X_dev
 
 def dense_gemm(W: torch.Tensor, X: torch.Tensor, out_dtype: torch.dtype | None = None, alpha: float = 1.0,
                out: torch.Tensor | None = None, bias: torch.Tensor | None = None, act: str = "none",
-               y_scale: float = 1.0):
-    """Y = round(y_scale * act(alpha * W . X + bias[:, None])) on the dense tensor cores."""
+               y_scale: float = 1.0, variant: int = 0):
+    """Y = round(y_scale * act(alpha * W . X + bias[:, None])) on the dense tensor cores.
+    variant != 0 forces a tile variant (dense_gemm_variant)."""
     dt = _DT[W.dtype]
     M, K = W.shape
     N = X.shape[1]
@@ -238,7 +247,10 @@ def dense_gemm(W: torch.Tensor, X: torch.Tensor, out_dtype: torch.dtype | None =
         out = torch.empty((M, N), dtype=out_dtype, device=X.device)
     ep = _epilogue(bias, act, y_scale, M)
     args = (dt, _DT[out.dtype], M, N, K, _p(W), W.stride(0), _p(X), X.stride(0), _p(out), out.stride(0), alpha)
-    if ep is None and out.dtype != torch.float8_e4m3fn:
+    if variant:
+        _check(lib.dense_gemm_variant(*args, None if ep is None else C.byref(ep), variant, _stream(X.device)),
+               "dense_gemm_variant")
+    elif ep is None and out.dtype != torch.float8_e4m3fn:
         _check(lib.dense_gemm(*args, _stream(X.device)), "dense_gemm")
     else:
         _check(lib.dense_gemm_ep(*args, None if ep is None else C.byref(ep), _stream(X.device)), "dense_gemm_ep")

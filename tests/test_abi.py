@@ -20,6 +20,40 @@ def ssdnn():
     return mod
 
 
+class Buffers:
+    """Operand addresses for calls that must be refused on the host. With a GPU
+    present they are real device allocations (64 KB each, 256-byte aligned, large
+    enough for every small shape used here), so that a refusal that regressed
+    would launch on valid memory; without one they are distinct dummy addresses,
+    which nothing can dereference because no kernel can run."""
+
+    def __init__(self):
+        import torch
+        self.cuda = torch.cuda.is_available()
+        self._keep = []
+        self._next = 1 << 20
+
+    def dev(self, nbytes: int = 1 << 16) -> int:
+        if self.cuda:
+            import torch
+            t = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+            self._keep.append(t)
+            return t.data_ptr()
+        self._next += max(nbytes, 256) + 4096
+        return self._next
+
+    def host(self, nbytes: int = 1 << 16) -> int:
+        a = np.zeros(max(nbytes, 256) + 256, dtype=np.uint8)
+        self._keep.append(a)
+        p = a.ctypes.data
+        return p + (-p % 256)
+
+
+@pytest.fixture
+def bufs():
+    return Buffers()
+
+
 def _declared():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
@@ -82,15 +116,16 @@ def test_tw_sizes_match_layout(ssdnn):
     assert e.value.status == 2
 
 
-def test_argument_errors_before_any_device_work(ssdnn):
+def test_argument_errors_before_any_device_work(ssdnn, bufs):
     lib = ssdnn.lib
+    d = [bufs.dev() for _ in range(6)]
     # bad dtype, negative sizes, K % 4 != 0: rejected on the host
     assert lib.sp24_prune_compress(9, None, 4, 8, 8, None, None, None, None) == 1
     assert lib.sp24_prune_compress(0, None, -1, 8, 8, None, None, None, None) == 1
     assert lib.sp24_prune_compress(0, None, 4, 6, 6, None, None, None, None) == 2
     assert lib.sp24_gemm(0, 2, 4, 4, 8, None, None, None, 4, None, 4, 1.0, None) == 2   # out e4m3
     assert lib.sp24_gemm(0, 0, 4, 4, 8, None, None, None, 4, None, 4, 1.0, None) == 1   # null Y
-    assert lib.dense_gemm(0, 0, 4, 8, 8, 16, 8, 16, 4, 32, 8, 1.0, None) == 1           # ldx < N
+    assert lib.dense_gemm(0, 0, 4, 8, 8, d[0], 8, d[1], 4, d[2], 8, 1.0, None) == 1     # ldx < N
     assert lib.tvw_gemm(2, 0, 4, 4, 8, None, None, None, None, None, None, None, 4, None, 4, None) == 2
     # empty problems are valid no-ops
     assert lib.sp24_gemm(0, 0, 0, 4, 8, None, None, None, 4, None, 4, 1.0, None) == 0
@@ -108,18 +143,23 @@ def test_argument_errors_before_any_device_work(ssdnn):
     assert lib.ssdnn_mma_rate_pair(2, 1, (1 << 18) + 1, None) == 1
     assert lib.ssdnn_mma_rate(1, 0, 96, 16, None) == 2
     # fused epilogue: unknown activation, non-finite scale, misaligned bias, e4m3 pitch
-    import ctypes as C
     ep = ssdnn.Epilogue(None, 5, 1.0)
-    assert lib.dense_gemm_ep(0, 0, 4, 8, 8, 16, 8, 16, 8, 16, 8, 1.0, C.byref(ep), None) == 1
+    assert lib.dense_gemm_ep(0, 0, 4, 8, 8, d[0], 8, d[1], 8, d[2], 8, 1.0, C.byref(ep), None) == 1
     ep = ssdnn.Epilogue(None, 1, float("inf"))
-    assert lib.sp24_gemm_ep(0, 0, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, C.byref(ep), None) == 1
-    ep = ssdnn.Epilogue(2, 1, 1.0)
-    assert lib.sp24_gemm_ep(0, 0, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, C.byref(ep), None) == 2
-    assert lib.sp24_gemm_ep(0, 2, 4, 8, 8, 16, 16, 16, 8, 16, 8, 1.0, None, None) == 2      # e4m3 row pitch 8 B
-    assert lib.sp24_gemm(0, 2, 4, 16, 8, 16, 16, 16, 16, 16, 16, 1.0, None) == 2          # plain call: no e4m3 out
+    assert lib.sp24_gemm_ep(0, 0, 4, 8, 8, d[0], d[3], d[1], 8, d[2], 8, 1.0, C.byref(ep), None) == 1
+    ep = ssdnn.Epilogue(d[4] + 2, 1, 1.0)                                                   # bias not 4-byte aligned
+    assert lib.sp24_gemm_ep(0, 0, 4, 8, 8, d[0], d[3], d[1], 8, d[2], 8, 1.0, C.byref(ep), None) == 2
+    assert lib.sp24_gemm_ep(0, 2, 4, 8, 8, d[0], d[3], d[1], 8, d[2], 8, 1.0, None, None) == 2  # e4m3 row pitch 8 B
+    assert lib.sp24_gemm(0, 2, 4, 16, 8, d[0], d[3], d[1], 16, d[2], 16, 1.0, None) == 2      # plain call: no e4m3 out
+    # explicit tile variants: unknown values, and variants the operand type lacks
+    assert lib.sp24_gemm_variant(1, 1, 4, 8, 8, d[0], d[3], d[1], 8, d[2], 8, 1.0, None, 1234, None) == 2
+    assert lib.sp24_gemm_variant(2, 1, 4, 16, 8, d[0], d[3], d[1], 16, d[2], 16, 1.0, None, 1064, None) == 2
+    assert lib.dense_gemm_variant(1, 1, 4, 8, 8, d[0], 8, d[1], 8, d[2], 8, 1.0, None, 19256, None) == 2
+    assert lib.dense_gemm_variant(1, 1, 4, 8, 8, d[0], 8, d[1], 8, d[2], 8, 1.0, None, 2192, None) == 2
     # the host-buffer GEMM: block height a multiple of 128, host buffers required
-    assert lib.sp24_gemm_host(1, 1, 256, 8, 64, 16, 16, 16, 8, 16, 8, 1.0, 16, 16, 100, None, None) == 1
-    assert lib.sp24_gemm_host(1, 1, 256, 8, 64, 16, 16, None, 8, 16, 8, 1.0, 16, 16, 128, None, None) == 1
+    hx, hy = bufs.host(), bufs.host()
+    assert lib.sp24_gemm_host(1, 1, 256, 8, 64, d[0], d[3], hx, 8, hy, 8, 1.0, d[1], d[2], 100, None, None) == 1
+    assert lib.sp24_gemm_host(1, 1, 256, 8, 64, d[0], d[3], None, 8, hy, 8, 1.0, d[1], d[2], 128, None, None) == 1
     # block-wise: K % 64, kept blocks within range, e4m3 unsupported
     k = np.array([1, 2], dtype=np.int32)
     assert lib.bw_sizes(1, 256, 100, k.ctypes.data_as(C.POINTER(C.c_int32)), None, None, None) == 2
@@ -138,9 +178,43 @@ def test_bw_sizes_match_layout(ssdnn):
     assert ssdnn.lib.ew_sizes(2, 8, 16, 4, None, None, None) == 2
 
 
-def test_conv_argument_checks(ssdnn):
+def test_conv_argument_checks(ssdnn, bufs):
     lib = ssdnn.lib
+    d = [bufs.dev() for _ in range(4)]
     # C_in not a multiple of 64, image wider than 224, e4m3
-    assert lib.sp24_conv3x3(1, 1, 128, 32, 1, 8, 8, 16, 16, 16, 16, 64, 1.0, None) == 2
-    assert lib.sp24_conv3x3(1, 1, 128, 64, 1, 8, 256, 16, 16, 16, 16, 2048, 1.0, None) == 2
-    assert lib.dense_conv3x3(2, 1, 128, 64, 1, 8, 8, 16, 576, 16, 16, 64, 1.0, None) == 2
+    assert lib.sp24_conv3x3(1, 1, 128, 32, 1, 8, 8, d[0], d[1], d[2], d[3], 64, 1.0, None) == 2
+    assert lib.sp24_conv3x3(1, 1, 128, 64, 1, 8, 256, d[0], d[1], d[2], d[3], 2048, 1.0, None) == 2
+    assert lib.dense_conv3x3(2, 1, 128, 64, 1, 8, 8, d[0], 576, d[2], d[3], 64, 1.0, None) == 2
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="host-only: the refused problems exceed the fixed scratch, so a regressed "
+                           "refusal must never reach a GPU")
+def test_noalloc_refusals_host_only(ssdnn):
+    """tw_prune_compress_noalloc refuses, before any CUDA call, problems beyond its
+    fixed limits: more than SSDNN_NOALLOC_MAX_TILES tiles (the kept counts travel
+    as a fixed-size kernel parameter), and more than SSDNN_NOALLOC_MAX_SCORES
+    scores. Dummy addresses only: nothing here may run on a device."""
+    lib = ssdnn.lib
+    max_tiles, max_scores = 2048, 1 << 21
+    hdr = open(HEADER).read()
+    assert f"#define SSDNN_NOALLOC_MAX_TILES {max_tiles}" in hdr
+    assert "#define SSDNN_NOALLOC_MAX_SCORES (1 << 21)" in hdr
+    P = C.POINTER(C.c_int32)
+    # nt = max_tiles + 1 tiles, K small (nt * K well inside the score scratch)
+    nt = max_tiles + 1
+    keep = np.full(nt, 4, dtype=np.int32)
+    st = lib.tw_prune_compress_noalloc(1, 0, 1 << 20, 128 * nt, 16, 16, keep.ctypes.data_as(P),
+                                       2 << 20, 3 << 20, 4 << 20, 5 << 20, None, None, None)
+    assert st == 2
+    # exactly max_tiles tiles passes the tile limit; it is then refused only for a null W
+    keep = np.full(max_tiles, 4, dtype=np.int32)
+    st = lib.tw_prune_compress_noalloc(1, 0, None, 128 * max_tiles, 16, 16, keep.ctypes.data_as(P),
+                                       2 << 20, 3 << 20, 4 << 20, 5 << 20, None, None, None)
+    assert st == 1
+    # two tiles whose scores exceed the scratch by one tile row
+    K = max_scores // 2 + 64
+    keep = np.array([64, 64], dtype=np.int32)
+    st = lib.tw_prune_compress_noalloc(1, 0, 1 << 20, 256, K, K, keep.ctypes.data_as(P),
+                                       2 << 20, 3 << 20, 4 << 20, 5 << 20, None, None, None)
+    assert st == 2

@@ -31,14 +31,11 @@ def _check(Y, ref, B, out_dt, rel, act, ys):
 @pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
 @pytest.mark.parametrize("act", ["none", "relu", "gelu"])
 @pytest.mark.parametrize("out_e4m3", [False, True])
-@pytest.mark.parametrize("tile", [None, "9256", "9256k2"])
-def test_sp24_gemm_epilogue(dt, act, out_e4m3, tile, monkeypatch):
-    """The fused epilogue on the shape's own tiles and on forced SM-pair tiles with
-    one- and two-step stages ("k2")."""
+@pytest.mark.parametrize("tile", [0, 9256, 19256])
+def test_sp24_gemm_epilogue(dt, act, out_e4m3, tile):
+    """The fused epilogue on the shape's own tiles (variant 0) and on forced SM-pair
+    tiles with one- and two-step stages (9256, 19256)."""
     ss = lib()
-    if tile:
-        monkeypatch.setenv("SSDNN_TILE", tile.split("k")[0])
-        monkeypatch.setenv("SSDNN_KX", "2" if tile.endswith("k2") else "1")
     M, N, K = 300, 264, 520
     W = rand_bits(610 + M, (M, K), dt, 0.5)
     X = rand_bits(620 + N, (K, N), dt, 1.0)
@@ -48,7 +45,8 @@ def test_sp24_gemm_epilogue(dt, act, out_e4m3, tile, monkeypatch):
     bias = _bias(7, M)
     f = ss.sp24_prune_compress(dev_tensor(W, dt), canonical_meta=False)
     Y, buf = guarded_output(M, N, TORCH_OUT[out_dt])
-    ss.sp24_gemm(f, dev_padded(X, dt), alpha=alpha, out=Y, bias=torch.from_numpy(bias).cuda(), act=act, y_scale=ys)
+    ss.sp24_gemm(f, dev_padded(X, dt), alpha=alpha, out=Y, bias=torch.from_numpy(bias).cuda(), act=act, y_scale=ys,
+                 variant=tile)
     torch.cuda.synchronize()
     assert ss.check_device_error() == 0
     v, m = oracle.sp24.compress(W, dt)

@@ -181,7 +181,7 @@ def test_mma_rate_microbenchmark_runs_clean(dt, sparse):
     assert ss.check_device_error() == 0
 
 
-# Every tile variant, forced through the tile override (MT * 1000 + BN; 9000 + BN
+# Every tile variant, forced through the variant entry points (MT * 1000 + BN; 9000 + BN
 # for an SM pair: two CTAs of a cluster run M = 256 MMAs, each holding 128 rows of
 # W and half of the X panel), on a shape with ragged M (the odd CTA of the last
 # pair has no rows), ragged N and a partial last K stage, and on a multi-wave shape.
@@ -189,14 +189,15 @@ FORCED_SHAPES = [(300, 264, 520), (2000, 8192, 256)]
 
 
 def _forced_tiles(dt, sparse):
-    tiles = ["1128", "1256", "9256"] + (["1064"] if dt != "e4m3" else [])
-    return tiles + (["2192", "9256k2"] if sparse else ["2256"])
+    """Every tile variant the operand type has (sp24_gemm_variant / dense_gemm_variant)."""
+    tiles = [1128, 1256, 9256] + ([1064] if dt != "e4m3" else [])
+    return tiles + ([2192, 19256] if sparse else [2256])
 
 
 @pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
 @pytest.mark.parametrize("shape", FORCED_SHAPES)
 @pytest.mark.parametrize("sparse", [True, False])
-def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
+def test_forced_tiles_within_bound(dt, shape, sparse):
     ss = lib()
     M, N, K = shape
     W = rand_bits(700 + M, (M, K), dt, 0.5)
@@ -213,14 +214,12 @@ def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
         B = oracle.gemm.bound(W, X, dt, alpha)
     Xd = dev_padded(X, dt)
     for tile in _forced_tiles(dt, sparse):
-        # "k2": SM-pair stages of two 128-byte K steps
-        monkeypatch.setenv("SSDNN_TILE", tile.split("k")[0])
-        monkeypatch.setenv("SSDNN_KX", "2" if tile.endswith("k2") else "1")
+        # 19256: SM-pair stages of two 128-byte K steps
         Y, buf = guarded_output(M, N, torch.bfloat16 if out_dt == "bf16" else torch.float16)
         if sparse:
-            ss.sp24_gemm(f, Xd, alpha=alpha, out=Y)
+            ss.sp24_gemm(f, Xd, alpha=alpha, out=Y, variant=tile)
         else:
-            ss.dense_gemm(dev_padded(W, dt), Xd, alpha=alpha, out=Y)
+            ss.dense_gemm(dev_padded(W, dt), Xd, alpha=alpha, out=Y, variant=tile)
         torch.cuda.synchronize()
         assert ss.check_device_error() == 0, tile
         _check_y(Y, Y_ref, B, out_dt, REL[dt])
@@ -228,16 +227,14 @@ def test_forced_tiles_within_bound(dt, shape, sparse, monkeypatch):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "e4m3"])
-@pytest.mark.parametrize("tile", [None, "1128", "9256", "9256k2"])
-def test_sp24_gemm_host_direct_output(dt, tile, monkeypatch):
+@pytest.mark.parametrize("shape", [(1000, 264, 512), (4096, 4104, 256)])
+def test_sp24_gemm_host_direct_output(dt, shape):
     """Y_dev None: the epilogue stores straight into page-locked host memory. The
-    result is bit-identical to the same tiles' device output, and nothing outside
-    the M x N view of the pinned buffer is written."""
+    result is bit-identical to the device output of the same shape (same tiles:
+    single-CTA tiles for the small shape, SM-pair tiles for the large one), and
+    nothing outside the M x N view of the pinned buffer is written."""
     ss = lib()
-    if tile:
-        monkeypatch.setenv("SSDNN_TILE", tile.split("k")[0])
-        monkeypatch.setenv("SSDNN_KX", "2" if tile.endswith("k2") else "1")
-    M, N, K = 1000, 264, 512
+    M, N, K = shape
     W = rand_bits(811, (M, K), dt, 0.5)
     X = rand_bits(812, (K, N), dt, 1.0)
     f = ss.sp24_prune_compress(dev_tensor(W, dt), canonical_meta=False)

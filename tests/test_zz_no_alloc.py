@@ -6,8 +6,10 @@ that must not call cudaMalloc/cudaFree). For them the library keeps the score
 scratch in a fixed device array. This test calls that entry point through the
 C ABI twice in a row, on two different weights, and checks each result against
 the ordinary entry point (which takes a caller workspace): offsets, indices,
-schedule, packed operand and metadata must be bit-identical. It also checks that
-a problem larger than the fixed scratch is refused. The file sorts last so that
+schedule, packed operand and metadata must be bit-identical, including on
+weights with several tiles of equal kept length (the schedule's tie order). The
+refusal of problems beyond the fixed limits is a host-only test in test_abi.py
+(no device may see a refused problem). The file sorts last so that
 a run stopping at the first failure has run every other test before it; it must
 also pass on its own in a fresh process.
 """
@@ -69,6 +71,10 @@ def test_noalloc_matches_ordinary_entry_point_two_calls_in_a_row():
     cases = [
         (512, 1024, np.array([256, 0, 516, 1024], dtype=np.int32), True),   # TVW, an empty and a full tile
         (300, 200, np.array([7, 0, 200], dtype=np.int32), False),          # TW, ragged M and L
+        # several tiles of equal length: the schedule's tie order (length
+        # descending, tile ascending) computed on the device must match the host's
+        (1000, 512, np.array([128, 64, 128, 64, 128, 0, 64, 128], dtype=np.int32), True),
+        (1024, 256, np.array([64, 64, 64, 64, 64, 64, 64, 64], dtype=np.int32), False),
     ]
     for i, (M, K, keep, tvw) in enumerate(cases):
         W = dev_tensor(rand_bits(9100 + i, (M, K), "bf16", 0.02), "bf16")
@@ -76,12 +82,3 @@ def test_noalloc_matches_ordinary_entry_point_two_calls_in_a_row():
         want = _call_ordinary(ss, W, keep, tvw)
         _same(got, want)
         assert ss.check_device_error() == 0
-
-
-def test_noalloc_refuses_problems_beyond_its_scratch():
-    ss = lib()
-    M, K = 256, (1 << 21) // 2 + 64        # 2 tiles x K floats > the fixed scratch
-    keep = np.array([64, 64], dtype=np.int32)
-    k = keep.ctypes.data_as(C.POINTER(C.c_int32))
-    st = ss.lib.tw_prune_compress_noalloc(1, 0, 16, M, K, K, k, 16, 16, 16, 16, None, None, None)
-    assert st == 2   # SSDNN_ERR_UNSUPPORTED, nothing launched
