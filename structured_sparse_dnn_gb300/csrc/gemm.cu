@@ -75,6 +75,7 @@ struct Params {
   int32_t conv_patches;                         // patches per image
   uint32_t conv_box_bytes;                      // bytes one activation box delivers
   int32_t y_direct;                             // Y is page-locked host memory: plain stores, no TMA
+  int32_t b3d;      // SM pairs: the B map is 3-D (64 columns, K rows, 64-column blocks), one box per stage
 };
 
 template <int DT, bool SPARSE, bool GATHER, int BN, int MT, int BROW = 128, bool PAIR = false,
@@ -150,6 +151,9 @@ struct Cfg {
   static constexpr int META_COLS = SPARSE ? META_SLOTS * META_SLOT_COLS : 0;
   static constexpr int NACC = (2 * ACC_COLS + META_COLS <= 512) ? 2 : 1;
   static constexpr int META_COL0 = NACC * ACC_COLS;         // TMEM columns after the accumulators
+  // the epilogue drains a single accumulator into registers before storing (at most
+  // four 32-column chunks per warp: 64 packed words per thread)
+  static constexpr bool EARLY_RELEASE = NACC == 1 && STAGED && BN / 32 / EPI_SPLIT <= 4;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC = ptx::idesc(Elem<DT>::mma_fmt, Elem<DT>::mma_fmt, SPARSE, PAIR ? 256 : 128,
                                                BN, false, !CONV);
@@ -443,10 +447,16 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
             if constexpr (SPARSE)  // one metadata block; past the last row block it reads zeros
               ptx::tma_load_2d_pair(sM, &tmM, bar, 0, (ui.meta_blk0 + KX * kb) * 16, pol_a);
             const int32_t n_half = ui.n0 + static_cast<int32_t>(crank & 1u) * C::BN_CTA;
+            if (C::B_BOXES > 1 && p.b3d) {
+              // all of this CTA's B boxes of the stage as one 3-D box: the layout
+              // [64-column block][K row][128 B] is the boxes' layout, B_BOX_BYTES apart
+              ptx::tma_load_3d_pair(sB, &tmB, bar_b, 0, kb * C::BK, n_half / C::B_BOX_COLS, pol_b);
+            } else {
 #pragma unroll
-            for (int bx = 0; bx < C::B_BOXES; ++bx)
-              ptx::tma_load_2d_pair(sB + bx * C::B_BOX_BYTES, &tmB, bar_b, n_half + bx * C::B_BOX_COLS,
-                                    kb * C::BK, pol_b);
+              for (int bx = 0; bx < C::B_BOXES; ++bx)
+                ptx::tma_load_2d_pair(sB + bx * C::B_BOX_BYTES, &tmB, bar_b, n_half + bx * C::B_BOX_COLS,
+                                      kb * C::BK, pol_b);
+            }
           } else {
           ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0u : (CONV ? p.conv_box_bytes : C::B_BYTES)) +
                                                        (SPARSE ? 2048 * ui.subs : 0));
@@ -702,8 +712,8 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
       const int c0 = half * NCH;
       const bool ragged_end = ((p.N * (p.out_dt == 2 ? 1 : 2)) & 15) != 0;
       const int32_t wrow0 = ui.m0 + static_cast<int32_t>(128 * mt + 32 * q);
-#pragma unroll 1
-      for (int c = c0; c < c0 + NCH; ++c) {
+      // chunk c of this warp's rows: TMEM -> fp32 epilogue -> packed output words
+      auto convert_chunk = [&](int c, uint32_t (&w)[16]) {
         uint32_t r[32];
         if (ui.nk > 0) {
           ptx::tmem_ld_32x32b_x32(
@@ -713,14 +723,6 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        if (c == c0 + NCH - 1) {  // this warp's part of the accumulator has been read: release it
-          ptx::tc_fence_before();
-          if (leader)
-            ptx::mbar_arrive(&acc_empty[acc]);
-          else  // the odd CTA of a pair releases its rows on the even CTA's barrier
-            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&acc_empty[acc]), crank & ~1u));
-        }
-        const int32_t n0 = ui.n0 + 32 * c;
         float x[32];
         if (plain_epilogue) {  // no bias, no activation, no output scale: one multiply
 #pragma unroll
@@ -730,21 +732,31 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           for (int i = 0; i < 32; ++i)
             x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, p.act, p.y_scale);
         }
-        uint32_t w[16];
         pack_row32(p.out_dt, x, w);
+      };
+      // this warp's part of the accumulator has been read: release it
+      auto release = [&]() {
+        ptx::tc_fence_before();
+        if (leader)
+          ptx::mbar_arrive(&acc_empty[acc]);
+        else  // the odd CTA of a pair releases its rows on the even CTA's barrier
+          ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&acc_empty[acc]), crank & ~1u));
+      };
+      auto store_chunk = [&](int c, const uint32_t (&w)[16]) {
+        const int32_t n0 = ui.n0 + 32 * c;
         if constexpr (C::STAGED) {
           if (p.y_direct) {  // host-memory output: each thread stores its row's chunk
             if (row_ok && n0 < p.N) store_packed_row32(yrow, n0, p.N, p.out_dt, w, pol_y);
-            continue;
+            return;
           }
           // this warp's 32 rows x 32 columns go through a staging buffer and a TMA
           // store, which clips rows past M and columns past N
-          if (ui.phantom || wrow0 >= p.M || n0 >= p.N) continue;  // uniform over the warp
+          if (ui.phantom || wrow0 >= p.M || n0 >= p.N) return;  // uniform over the warp
           if (ragged_end && n0 + 32 > p.N) {
             // a row end that is not a multiple of 16 bytes: the copy engine writes
             // whole 16-byte units there, so that chunk is stored directly
             if (row_ok) store_packed_row32(yrow, n0, p.N, p.out_dt, w, pol_y);
-            continue;
+            return;
           }
           uint8_t* buf = staging + (warp - C::EPI_WARP0) * (2048 * C::STAGING_BUFS) +
                          (C::STAGING_BUFS == 2 ? (chunk_seq & 1) * 2048 : 0);
@@ -767,8 +779,27 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
         } else {
           // convolution patches end at their last valid image row
           const int32_t n_lim = CONV ? ui.n0 + ui.ncols : p.N;
-          if (!row_ok || n0 >= n_lim) continue;
+          if (!row_ok || n0 >= n_lim) return;
           store_packed_row32(yrow, n0, n_lim, p.out_dt, w, pol_y);
+        }
+      };
+      if constexpr (C::EARLY_RELEASE) {
+        // single accumulator: read all of this warp's chunks into packed registers and
+        // release the accumulator before any store, so the next tile's MMAs (and the
+        // producer behind them) wait only for the TMEM reads
+        uint32_t wk[NCH][16];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) convert_chunk(c0 + i, wk[i]);
+        release();
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) store_chunk(c0 + i, wk[i]);
+      } else {
+#pragma unroll 1
+        for (int c = c0; c < c0 + NCH; ++c) {
+          uint32_t w[16];
+          convert_chunk(c, w);
+          if (c == c0 + NCH - 1) release();
+          store_chunk(c, w);
         }
       }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
@@ -842,6 +873,24 @@ bool make_map_nhwc(CUtensorMap* m, const void* base, uint64_t C_, uint64_t W_, u
   return r == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over a row-major 16-bit matrix of K rows seen as (64 columns,
+// K rows, nblk 64-column blocks) -- strides row pitch and 128 bytes -- with boxes of
+// 64 x box_rows x box_blks, 128B swizzle: one box lands as box_blks 64-column boxes
+// of box_rows 128-byte rows, one after another.
+bool make_map_3d_blocks(CUtensorMap* m, const void* base, uint64_t rows, uint64_t nblk, uint64_t pitch_bytes,
+                        uint32_t box_rows, uint32_t box_blks) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, rows, nblk};
+  const cuuint64_t strides[2] = {pitch_bytes, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_blks};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -856,6 +905,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   const int eb = C::EB;
   CUtensorMap tA, tB, tM;
   bool ok;
+  bool b3d = false;
   int32_t conv_rows = 0;
   if constexpr (CONV) {
     // A as for the 2:4 / dense GEMM over the flattened filter; X as NHWC boxes of
@@ -883,8 +933,15 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
                     CU_TENSOR_MAP_SWIZZLE_64B);
     else
       ok = make_map(&tA, a.A, eb, a.K, a.M, a.lda * eb, 128 / eb, C::BM, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::BK,
-                        BROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (PAIR && C::B_BOXES > 1 && BROW == 128 && a.N % C::B_BOX_COLS == 0) {
+      // X seen as (64 columns, K rows, N / 64 blocks): one box per stage brings all of
+      // this CTA's B boxes; every element it addresses lies inside the matrix
+      b3d = ok && make_map_3d_blocks(&tB, a.X, a.K, a.N / C::B_BOX_COLS, a.ldx * eb, C::BK, C::B_BOXES);
+    }
+    if (!b3d) {
+      ok = ok && make_map(&tB, a.X, eb, a.N, a.K, a.ldx * eb, C::B_BOX_COLS, C::BK,
+                          BROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    }
   } else {
     // packed operand seen as (packed_rows x 64) dense or (packed_rows x 32) values
     if constexpr (SPARSE)
@@ -972,6 +1029,7 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
   p.ldy = a.ldy;
   p.err = err;
   p.y_direct = y_host ? 1 : 0;
+  p.b3d = b3d ? 1 : 0;
   if (p.num_units == 0) return cudaSuccess;
 
   auto kern = k_gemm<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BLOCKW, CONV, KX>;
