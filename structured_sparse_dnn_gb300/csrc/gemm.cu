@@ -99,7 +99,8 @@ struct Cfg {
   static constexpr int BM = 128 * MT;
   // 4 control warps, 4 epilogue warps per sub-tile, and for TW/TVW 4 warps that
   // gather the kept X rows with 16-byte cp.async
-  static constexpr int GATHER_THREADS = GATHER ? 128 : 0;
+  static constexpr int GATHER_WARPS = 16;
+  static constexpr int GATHER_THREADS = GATHER ? 32 * GATHER_WARPS : 0;
   // SM pairs drain their 128 x 256 accumulator with eight epilogue warps (two per
   // TMEM lane quadrant, each taking half of the columns)
   static constexpr int EPI_SPLIT = PAIR ? 2 : 1;
@@ -107,11 +108,6 @@ struct Cfg {
   static constexpr int EPI_WARP0 = 4;
   static constexpr int GATHER_WARP0 = 4 + EPI_WARPS;
   static constexpr int THREADS = 128 + 32 * EPI_WARPS + GATHER_THREADS;
-  static constexpr int STAGES_FOR_LAG = ((220 * 1024) / (MT * (SPARSE ? 128 * 64 : 128 * 128) + 128 * BN +
-                                                           (SPARSE ? 2048 * MT : 0)));
-  // stages a gather thread keeps in flight before it must see its oldest copies land
-  // (a larger lag keeps more copies in flight but fewer landed stages ready for the MMA)
-  static constexpr int GATHER_LAG = STAGES_FOR_LAG >= 8 ? 2 : 1;
   static constexpr int EB = Elem<DT>::bytes;
   static constexpr bool F8 = Elem<DT>::f8;
   // KX = 2 (2:4 on SM pairs): a stage holds two 128-byte K steps, so every
@@ -537,6 +533,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
         if (KX == 2 && lane == 0 && ok) ok = wait_bounded(&full_b[stage], phase, p.err);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) { *abort_flag = 1; break; }
+        // TW/TVW: the gathered rows were written by cp.async (generic proxy); order them
+        // before the tensor core's reads (async proxy)
+        if constexpr (GATHER) ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t sA = ptx::smem_u32(smem + stage * C::STAGE_BYTES);
@@ -621,35 +620,36 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
     __syncwarp();
   } else if (GATHER && warp >= C::GATHER_WARP0) {
     // ------------------------------------------------------------ X-row gather (TW/TVW)
-    // Gather warp w copies stage rows r = 4 i + w (i < 16). Lanes take consecutive
+    // Gather warp w copies stage rows r = GW i + w (i < 64 / GW). Lanes take consecutive
     // 16-byte chunks of a row (a warp instruction copies 512 contiguous bytes of X:
     // one row for a 256-wide N tile, two rows for 128), straight into the
     // 128B-swizzled MN-major operand layout; rows past L_t and columns past N are
-    // zero-filled. A thread arrives on a stage's full barrier GATHER_LAG stages
-    // later, after waiting for its own copies of that stage and fencing them for
-    // the tensor core's async proxy.
+    // zero-filled. Each thread's copies of a stage complete on the stage's full
+    // barrier by themselves (cp.async.mbarrier.arrive), so the gather runs ahead
+    // by the whole ring; the MMA thread fences them for the tensor core's async
+    // proxy after its wait.
     const int w = warp - C::GATHER_WARP0;
     constexpr int CPR = BN / 8;                      // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;                    // rows per warp instruction
-    constexpr int ITERS = 16 / RPI;                  // instructions per stage
+    constexpr int GW = C::GATHER_WARPS;
+    constexpr int ROWS_W = 64 / GW;                  // stage rows per gather warp
+    constexpr int ITERS = ROWS_W / RPI;              // instructions per stage
     const int sub = static_cast<int>(lane) / CPR, q = static_cast<int>(lane) % CPR;
     const int col = 8 * q;                           // column within the N tile
     const int bx = col >> 6, cc = (col & 63) >> 3;   // 64-column box, 16-byte chunk in its row
     constexpr int kIdxAhead = 3;
     int stage = 0;
     uint32_t phase = 0;
-    int lag_stage[C::GATHER_LAG + 1];
-    int pending = 0;
     bool ok = true;
     const uint16_t* X = static_cast<const uint16_t*>(p.X);
-    int32_t idx_ring[kIdxAhead];                     // lane l < 16: X row of stage row 4 l + w
+    int32_t idx_ring[kIdxAhead];                     // lane l < ROWS_W: X row of stage row GW l + w
     for (int32_t r = 0, u = unit_at(0); u >= 0 && ok; u = unit_at(++r)) {
       const UnitInfo ui = decode_unit<C, C::SCHEDULED>(p, u, crank);
       const int32_t gcol = ui.n0 + col;
       const uint32_t col_bytes = gcol >= p.N ? 0u : static_cast<uint32_t>(min(8, p.N - gcol) * 2);
       auto row_of = [&](int32_t kb) -> int32_t {
-        const int32_t j = kb * C::BK + 4 * static_cast<int32_t>(lane) + w;
-        return (lane < 16 && kb < ui.nk && j < ui.L) ? __ldg(p.indices + ui.idx_base + j) : -1;
+        const int32_t j = kb * C::BK + GW * static_cast<int32_t>(lane) + w;
+        return (lane < ROWS_W && kb < ui.nk && j < ui.L) ? __ldg(p.indices + ui.idx_base + j) : -1;
       };
 #pragma unroll
       for (int d = 0; d < kIdxAhead; ++d) idx_ring[d] = row_of(d);
@@ -661,32 +661,21 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
         uint8_t* sB = smem + stage * C::STAGE_BYTES + C::A_BYTES;
 #pragma unroll
         for (int i = 0; i < ITERS; ++i) {
-          const int ri = i * RPI + sub;              // warp-local row 0..15
-          const int r = 4 * ri + w;                  // stage row 0..63
+          const int ri = i * RPI + sub;              // warp-local row 0 .. ROWS_W - 1
+          const int r = GW * ri + w;                 // stage row 0..63
           const int32_t xrow = __shfl_sync(0xffffffffu, idx_ring[0], ri);
           const uint32_t bytes = xrow < 0 ? 0u : col_bytes;
           const uint16_t* src = bytes ? X + static_cast<int64_t>(xrow) * p.ldx + gcol : X;
           ptx::cp_async_16(sB + bx * C::B_BOX_BYTES + r * 128 + ((cc ^ (r & 7)) << 4), src, bytes);
         }
-        ptx::cp_async_commit();
+        ptx::cp_async_mbar_arrive_noinc(&full[stage]);
 #pragma unroll
         for (int d = 0; d + 1 < kIdxAhead; ++d) idx_ring[d] = idx_ring[d + 1];
         idx_ring[kIdxAhead - 1] = row_of(kb + kIdxAhead);
-        lag_stage[pending++] = stage;
-        if (pending > C::GATHER_LAG) {
-          ptx::cp_async_wait<C::GATHER_LAG>();
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(&full[lag_stage[0]]);
-#pragma unroll
-          for (int d = 0; d < C::GATHER_LAG; ++d) lag_stage[d] = lag_stage[d + 1];
-          --pending;
-        }
         if (++stage == p.nstages) { stage = 0; phase ^= 1u; }
       }
     }
-    ptx::cp_async_wait<0>();
-    ptx::fence_proxy_async_smem();
-    for (int d = 0; d < pending; ++d) ptx::mbar_arrive(&full[lag_stage[d]]);
+    ptx::cp_async_wait<0>();  // no copy of this thread is still writing shared memory
   } else if (warp >= C::EPI_WARP0 && warp < C::EPI_WARP0 + C::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp & 3u;                 // TMEM lane quadrant this warp may read
