@@ -325,6 +325,9 @@ int bw_gemm_ep(int dt, int out_dt, int64_t M, int64_t N, int64_t K, const int32_
  *   2256   256 x 256 tiles, one CTA with two M = 128 instructions (dense only)
  *   9256   256 x 256 tiles on an SM pair (cta_group::2), one 128-byte K step per stage
  *   19256  the same with two K steps per stage (2:4 only)
+ *   11064, 11128  1064 / 1128 with two 128-byte K steps of the compressed weight per
+ *          stage (2:4 only; 11064 fp16/bf16 only)
+ * (For 2:4, 1064 and 1128 run one K step per stage; the plain calls pick two.)
  * Any other value, or one the operand type does not have: SSDNN_ERR_UNSUPPORTED,
  * before any work is enqueued. The pages have no counterpart: this selects among
  * implementations of the same product. */

@@ -163,7 +163,10 @@ struct Cfg {
   static_assert(!CONV || (!GATHER && !PAIR && !BLOCKW && MT == 1 && Elem<DT>::bytes == 2),
                 "convolution: 16-bit, 128-row tiles");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
-  static_assert(KX == 1 || (KX == 2 && SPARSE && PAIR), "double K stages: 2:4 on SM pairs");
+  static_assert(KX == 1 || (KX == 2 && SPARSE && MT == 1 && !GATHER && !CONV && !BLOCKW),
+                "double K stages: 2:4 tiles of 128 rows (one CTA or an SM pair)");
+  // SM pairs with two-step stages take their X boxes on a second barrier
+  static constexpr bool B_OWN_BARRIER = PAIR && KX == 2;
   static_assert(MT == 1 || !GATHER, "256-row tiles: no gather");
 };
 
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
   // KX = 2: the X boxes of a stage complete on a second barrier, so that neither
   // barrier expects more than 64 KB per phase
   uint64_t* full_b = drain + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full_b + (KX == 2 ? C::STAGES : 0));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full_b + (C::B_OWN_BARRIER ? C::STAGES : 0));
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const uint32_t warp = threadIdx.x >> 5;
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(&full[s], 1 + C::GATHER_THREADS);
       ptx::mbar_init(&empty[s], 1);
-      if constexpr (KX == 2) ptx::mbar_init(&full_b[s], 1);
+      if constexpr (C::B_OWN_BARRIER) ptx::mbar_init(&full_b[s], 1);
     }
     for (int a = 0; a < C::NACC; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
@@ -454,8 +457,11 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
                                       kb * C::BK, pol_b);
             }
           } else {
+          // 2:4 metadata blocks of the stage (KX per sub-tile; the last stage of a row
+          // block may cover only one of two)
+          const int32_t meta_n = SPARSE ? min(KX, p.meta_kb - KX * kb) : 0;
           ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0u : (CONV ? p.conv_box_bytes : C::B_BYTES)) +
-                                                       (SPARSE ? 2048 * ui.subs : 0));
+                                                       static_cast<uint32_t>(2048 * meta_n * ui.subs));
           // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
           // rows past M read as zeros
           const int32_t a_col = C::SCHEDULED ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
@@ -463,8 +469,10 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           ptx::tma_load_2d(sA, &tmA, &full[stage], a_col, a_row, pol_a);
           if constexpr (SPARSE) {
             for (int mt = 0; mt < ui.subs; ++mt) {
-              const uint8_t* src = p.meta_hw + static_cast<int64_t>(ui.meta_blk0 + mt * ui.nk + kb) * 2048;
-              ptx::bulk_load(sM + mt * 2048, src, 2048, &full[stage], pol_a);
+              // sub-tile mt's blocks follow the row block's meta_kb blocks (TW/TVW tiles: nk)
+              const int32_t stride = C::SCHEDULED ? ui.nk : p.meta_kb;
+              const uint8_t* src = p.meta_hw + static_cast<int64_t>(ui.meta_blk0 + mt * stride + KX * kb) * 2048;
+              ptx::bulk_load(sM + mt * 2048 * KX, src, static_cast<uint32_t>(2048 * meta_n), &full[stage], pol_a);
             }
           }
           if constexpr (CONV) {
@@ -508,7 +516,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
       for (int n = 0; n < pending; ++n) {
         if (--s < 0) { s = p.nstages - 1; ph ^= 1u; }
         wait_bounded(&full[s], ph, nullptr);
-        if constexpr (KX == 2) wait_bounded(&full_b[s], ph, nullptr);
+        if constexpr (C::B_OWN_BARRIER) wait_bounded(&full_b[s], ph, nullptr);
       }
     }
   } else if (warp == 1 && leader) {
@@ -530,7 +538,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
       uint32_t cur_meta = 0;
       for (int32_t kb = 0; kb < ui.nk; ++kb) {
         if (lane == 0) ok = wait_bounded(&full[stage], phase, p.err);
-        if (KX == 2 && lane == 0 && ok) ok = wait_bounded(&full_b[stage], phase, p.err);
+        if (C::B_OWN_BARRIER && lane == 0 && ok) ok = wait_bounded(&full_b[stage], phase, p.err);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) { *abort_flag = 1; break; }
         // TW/TVW: the gathered rows were written by cp.async (generic proxy); order them
@@ -1098,7 +1106,9 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
     // large 16-bit 2:4 problems: SM pairs with two-step stages (measured ahead of
     // the 256 x 192 single-CTA tiles the fill model picks there)
     if (sparse && EB == 2 && c.mt == 2 && c.bn == 192) c = TileChoice{1, 256, true};
-    int kx = 2;  // 2:4 SM-pair tiles: stages of two 128-byte K steps
+    // 2:4 tiles of 128 rows: stages of two 128-byte K steps (half the serial K loop of
+    // one-step stages) on SM pairs and on single CTAs up to 128 columns
+    int kx = 2;
     if (a.variant) {  // an explicit tile variant (validated by the caller)
       const int v = a.variant % 10000;
       c = TileChoice{v / 1000 == 9 ? 1 : v / 1000, v % 1000, v / 1000 == 9};
@@ -1129,12 +1139,20 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
       return cudaErrorInvalidValue;
     }
     if (c.bn == 64) {
-      if constexpr (EB == 2)
-        return sparse ? run<DT, true, false, 64>(a, s, err) : run<DT, false, false, 64>(a, s, err);
+      if constexpr (EB == 2) {
+        if (sparse)
+          return kx == 2 ? run<DT, true, false, 64, 1, 128, false, false, false, 2>(a, s, err)
+                         : run<DT, true, false, 64>(a, s, err);
+        return run<DT, false, false, 64>(a, s, err);
+      }
       return cudaErrorInvalidValue;
     }
-    if (c.bn == 128)
-      return sparse ? run<DT, true, false, 128>(a, s, err) : run<DT, false, false, 128>(a, s, err);
+    if (c.bn == 128) {
+      if (sparse)
+        return kx == 2 ? run<DT, true, false, 128, 1, 128, false, false, false, 2>(a, s, err)
+                       : run<DT, true, false, 128>(a, s, err);
+      return run<DT, false, false, 128>(a, s, err);
+    }
     return sparse ? run<DT, true, false, 256>(a, s, err) : run<DT, false, false, 256>(a, s, err);
   }
   if (mode == 5 || mode == 6) {
@@ -1199,7 +1217,8 @@ bool gemm_variant_ok(int variant, bool sparse, int elem_bytes) {
   switch (variant) {
     case 0: case 1128: case 1256: case 9256: return true;
     case 1064: return elem_bytes == 2;
-    case 2192: case 19256: return sparse;
+    case 11064: return sparse && elem_bytes == 2;
+    case 2192: case 11128: case 19256: return sparse;
     case 2256: return !sparse;
   }
   return false;

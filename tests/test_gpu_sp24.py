@@ -191,7 +191,9 @@ FORCED_SHAPES = [(300, 264, 520), (2000, 8192, 256)]
 def _forced_tiles(dt, sparse):
     """Every tile variant the operand type has (sp24_gemm_variant / dense_gemm_variant)."""
     tiles = [1128, 1256, 9256] + ([1064] if dt != "e4m3" else [])
-    return tiles + ([2192, 19256] if sparse else [2256])
+    if sparse:
+        tiles += [2192, 19256, 11128] + ([11064] if dt != "e4m3" else [])
+    return tiles + ([] if sparse else [2256])
 
 
 @pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3"])
