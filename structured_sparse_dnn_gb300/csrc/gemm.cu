@@ -246,16 +246,32 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
   return ui;
 }
 
+// GELU in its exact form x Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), with erf from the
+// rational approximation of Abramowitz and Stegun, Handbook of Mathematical
+// Functions, formula 7.1.26 (|error| <= 1.5e-7 for z >= 0):
+//   erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2), t = 1 / (1 + p z).
+// With q = (a1 t + ... + a5 t^5) exp(-z^2) and z = |x| / sqrt 2, 1 + erf(x / sqrt 2) is
+// 2 - q for x >= 0 and q for x < 0 (taken as q itself, so no cancellation there).
+__device__ __forceinline__ float gelu_exact(float x) {
+  constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
+                  kA4 = -1.453152027f, kA5 = 1.061405429f;
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = __fdividef(1.f, fmaf(kP, z, 1.f));
+  const float poly = t * fmaf(fmaf(fmaf(fmaf(kA5, t, kA4), t, kA3), t, kA2), t, kA1);
+  const float q = poly * __expf(-z * z);
+  return 0.5f * x * (x >= 0.f ? 2.f - q : q);
+}
+
 // The fused layer epilogue on one fp32 accumulator value, in this order: alpha
 // times the accumulator plus the row's bias (one fma), the activation, the
-// output scale. GELU is the exact form 0.5 x (1 + erf(x / sqrt 2)).
+// output scale.
 __device__ __forceinline__ float epilogue_value(float acc, float alpha, float b, bool has_bias, int act,
                                                float y_scale) {
-  float x = has_bias ? fmaf(acc, alpha, b) : acc * alpha;
+  float x = has_bias ? fmaf(acc, alpha, b) : acc * alpha;  // has_bias is uniform: no divergence
   if (act == 1) {
     x = x > 0.f ? x : 0.f;
   } else if (act == 2) {
-    x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+    x = gelu_exact(x);
   }
   return x * y_scale;
 }
@@ -709,25 +725,34 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
       const int c0 = half * NCH;
       const bool ragged_end = ((p.N * (p.out_dt == 2 ? 1 : 2)) & 15) != 0;
       const int32_t wrow0 = ui.m0 + static_cast<int32_t>(128 * mt + 32 * q);
-      // chunk c of this warp's rows: TMEM -> fp32 epilogue -> packed output words
-      auto convert_chunk = [&](int c, uint32_t (&w)[16]) {
-        uint32_t r[32];
+      // chunk c of this warp's rows: TMEM -> raw fp32 accumulator bits (call
+      // tmem_ld_wait before using them)
+      auto load_chunk = [&](int c, uint32_t (&r)[32]) {
         if (ui.nk > 0) {
           ptx::tmem_ld_32x32b_x32(
               tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS + mt * BN + 32 * c), r);
-          ptx::tmem_ld_wait();
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
+      };
+      // raw accumulator bits -> fp32 epilogue -> packed output words
+      auto convert_raw = [&](const uint32_t (&r)[32], uint32_t (&w)[16]) {
         float x[32];
+        // the activation is chosen once per chunk, so each branch is straight-line
+        // code over 32 independent values
         if (plain_epilogue) {  // no bias, no activation, no output scale: one multiply
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]) * p.alpha;
+        } else if (p.act == 2) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, 2, p.y_scale);
+        } else if (p.act == 1) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, 1, p.y_scale);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, p.act, p.y_scale);
+          for (int i = 0; i < 32; ++i) x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, 0, p.y_scale);
         }
         pack_row32(p.out_dt, x, w);
       };
@@ -781,21 +806,36 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
         }
       };
       if constexpr (C::EARLY_RELEASE) {
-        // single accumulator: read all of this warp's chunks into packed registers and
-        // release the accumulator before any store, so the next tile's MMAs (and the
-        // producer behind them) wait only for the TMEM reads
-        uint32_t wk[NCH][16];
+        // single accumulator: read all of this warp's chunks raw into registers and
+        // release the accumulator before the epilogue arithmetic and the stores, so
+        // the next tile's MMAs (and the producer behind them) wait only for the
+        // TMEM reads
+        uint32_t raw[NCH][32];
 #pragma unroll
-        for (int i = 0; i < NCH; ++i) convert_chunk(c0 + i, wk[i]);
+        for (int i = 0; i < NCH; ++i) load_chunk(c0 + i, raw[i]);
+        ptx::tmem_ld_wait();
         release();
+        // the epilogue arithmetic starts after the release: the raw values pass through
+        // an (empty) volatile asm placed after it, so the compiler cannot hoist the
+        // arithmetic above the release
 #pragma unroll
-        for (int i = 0; i < NCH; ++i) store_chunk(c0 + i, wk[i]);
+        for (int i = 0; i < NCH; ++i)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(raw[i][j]));
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          uint32_t w[16];
+          convert_raw(raw[i], w);
+          store_chunk(c0 + i, w);
+        }
       } else {
 #pragma unroll 1
         for (int c = c0; c < c0 + NCH; ++c) {
-          uint32_t w[16];
-          convert_chunk(c, w);
+          uint32_t r[32], w[16];
+          load_chunk(c, r);
+          ptx::tmem_ld_wait();
           if (c == c0 + NCH - 1) release();
+          convert_raw(r, w);
           store_chunk(c, w);
         }
       }
