@@ -272,6 +272,25 @@ int sp24_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int6
 int dense_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W, const void* Wf,
                   int64_t ldw, const void* X, void* Y, int64_t ldy, float alpha, void* stream);
 
+/* The 3x3 convolution with a tile-wise (TW) filter ("Accelerating Sparse DNNs Based
+ * on Tiled GEMM", Abstract: whole K-rows pruned per output tile of the GEMM, the
+ * skip made where operands are fetched from global memory; "SparseRT", Abstract:
+ * sparse 3x3 convolutions). Reading: the implicit GEMM fetches its activation
+ * operand in units of one filter tap x 64 input channels (one TMA box of NHWC
+ * data), so a 128-channel output tile keeps whole K-row groups of one tap and 64
+ * channels; a finer group would need 2-byte strided gathers of NHWC activations.
+ * Group g of the flattened filter (Cout x 9 Cin, column (r 3 + s) Cin + c) covers
+ * columns 64 g .. 64 g + 63, i.e. tap g / (Cin / 64) and channels
+ * 64 (g % (Cin / 64)) ..; its score is the fp32 sum of its 64 columns' TW scores.
+ * The compressed filter is exactly bw_prune_compress of the flattened filter with
+ * keep_blocks_host = keep_groups_host (kept groups per 128-channel tile); this call
+ * takes that form (the same offsets, indices, schedule and packed operand).
+ * Y as for sp24_conv3x3; a tile that keeps no group writes zeros. Cin % 64 == 0 and
+ * W <= 224, else SSDNN_ERR_UNSUPPORTED; fp16 / bf16 only. */
+int tw_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W,
+               const int32_t* keep_groups_host, const int32_t* offsets, const int32_t* indices, const int32_t* schedule,
+               const void* packed, const void* X, void* Y, int64_t ldy, float alpha, void* stream);
+
 /* --------------------------------------------------- fused layer epilogue ----
  * A pruned fully connected layer or 1x1 convolution runs as one of the GEMMs
  * above ("Accelerating Sparse DNNs Based on Tiled GEMM", Abstract), and the step

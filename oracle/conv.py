@@ -13,13 +13,20 @@ Readings where the pages are silent (each also listed in the design notes):
     of one tap), i.e. it is the 2:4 compression of the flattened filter;
   * Y[co, (n H + h) W + w] = alpha * sum_{r, s, c} W[co, r, s, c] X[n, h + r - 1, w + s - 1, c]
     (zero outside the image): the output is C_out x (N H W), channel-major;
-  * numerics as the GEMM: fp64 sum, one rounding to the output type.
+  * numerics as the GEMM: fp64 sum, one rounding to the output type;
+  * tile-wise filter ("Accelerating Sparse DNNs Based on Tiled GEMM", Abstract:
+    whole K-rows of the GEMM pruned per output tile, the skip made where operands
+    are fetched): a 128-channel output tile keeps whole K-row groups of one tap and
+    64 input channels (the unit in which the implicit GEMM fetches activations);
+    group g is columns 64 g .. 64 g + 63 of the flattened filter, scored by the fp32
+    sum of its columns' tile-wise scores -- the block-wise selection of bw.prune with
+    64-column blocks -- and the convolution uses the filter masked to those groups.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import codecs, gemm, sp24
+from . import bw, codecs, gemm, sp24
 
 
 def im2col(X: np.ndarray) -> np.ndarray:
@@ -47,6 +54,17 @@ def conv3x3(Wf: np.ndarray, X: np.ndarray, dt: str, out_dt: str, alpha: float = 
     Y = gemm.dense_product(Wf, cols, dt, alpha)
     B = gemm.bound(Wf, cols, dt, alpha)
     return codecs.encode(Y, out_dt), B
+
+
+def conv3x3_tw(Wf: np.ndarray, X: np.ndarray, dt: str, out_dt: str, keep_groups, alpha: float = 1.0):
+    """Y bits and bound for the tile-wise filter: per 128-channel tile t the first
+    keep_groups[t] (tap, 64-channel) groups by score (ties to the lower group), the
+    rest of the filter zero. Returns (Y, B, form) with form = bw.prune's output."""
+    keep = np.asarray(keep_groups, dtype=np.int64)
+    form = bw.prune(Wf, dt, keep)
+    masked = bw.masked_dense(Wf, form, keep)
+    Y, B = conv3x3(masked, X, dt, out_dt, alpha, sparse=False)
+    return Y, B, form
 
 
 def conv3x3_direct(Wf: np.ndarray, X: np.ndarray, dt: str) -> np.ndarray:

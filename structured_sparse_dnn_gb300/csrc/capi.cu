@@ -713,6 +713,48 @@ static int conv_impl(int sparse, int dt, int out_dt, int64_t Cout, int64_t Cin, 
   return from_cuda(launch_gemm(sparse ? 5 : 6, a, s, error_word()));
 }
 
+int tw_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W,
+               const int32_t* keep_groups_host, const int32_t* offsets, const int32_t* indices, const int32_t* schedule,
+               const void* packed, const void* X, void* Y, int64_t ldy, float alpha, void* stream) {
+  if (dt != SSDNN_F16 && dt != SSDNN_BF16) return dt == SSDNN_E4M3 ? SSDNN_ERR_UNSUPPORTED : SSDNN_ERR_INVALID_ARG;
+  if (Cout < 0 || Cin < 0 || Nb < 0 || H < 0 || W < 0) return SSDNN_ERR_INVALID_ARG;
+  if (Cout > kMaxDim || Nb * H * W > kMaxDim || 9 * Cin > kMaxDim || H > kMaxDim) return SSDNN_ERR_INVALID_ARG;
+  if (Cin % 64 || W > 224) return SSDNN_ERR_UNSUPPORTED;
+  const int64_t M = Cout, N = Nb * H * W, K = 9 * Cin;
+  int st = check_gemm_io(out_dt, false, M, N, K, X, round_up(N, 8), 2, Y, ldy);
+  if (st != SSDNN_OK || M == 0 || N == 0) return st;
+  if (!keep_groups_host) return SSDNN_ERR_INVALID_ARG;
+  BwTables tb;
+  st = build_bw_tables(M, K, keep_groups_host, &tb);  // a group is one tap x 64 channels: 64 columns of K
+  if (st != SSDNN_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0 || tb.n_blocks == 0) return zero_output(Y, ldy, M, N, 2, s);
+  if (!offsets || !indices || !schedule || !packed) return SSDNN_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return SSDNN_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.dt = dt;
+  a.out_dt = out_dt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = packed;
+  a.X = X;
+  a.ldx = N;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.alpha = alpha;
+  a.nt = tb.cols.t.nt;
+  a.packed_rows = 2 * tb.cols.t.P_total;
+  a.offsets = offsets;
+  a.indices = indices;
+  a.schedule = schedule;
+  a.conv_cin = Cin;
+  a.conv_h = H;
+  a.conv_w = W;
+  a.conv_nb = Nb;
+  return from_cuda(launch_gemm(7, a, s, error_word()));
+}
+
 int sp24_conv3x3(int dt, int out_dt, int64_t Cout, int64_t Cin, int64_t Nb, int64_t H, int64_t W, const void* values,
                  const uint8_t* meta_hw, const void* X, void* Y, int64_t ldy, float alpha, void* stream) {
   return conv_impl(1, dt, out_dt, Cout, Cin, Nb, H, W, values, 0, meta_hw, X, Y, ldy, alpha, stream);

@@ -73,6 +73,7 @@ struct Params {
   // 3x3 convolution: image geometry and the pixel patch of one work unit
   int32_t conv_cin, conv_h, conv_w, conv_rows;  // C_in, H, W, image rows per patch
   int32_t conv_patches;                         // patches per image
+  int32_t conv_nb;                              // images
   uint32_t conv_box_bytes;                      // bytes one activation box delivers
   int32_t y_direct;                             // Y is page-locked host memory: plain stores, no TMA
   int32_t b3d;      // SM pairs: the B map is 3-D (64 columns, K rows, 64-column blocks), one box per stage
@@ -160,7 +161,7 @@ struct Cfg {
   static_assert(BN % 32 == 0, "the epilogue drains 32-column chunks");
   static_assert(!PAIR || (MT == 1 && !GATHER), "SM pairs: one 128-row sub-tile per CTA");
   static_assert(!BLOCKW || (!SPARSE && !GATHER && !PAIR && MT == 1), "block-wise: dense 128-row tiles");
-  static_assert(!CONV || (!GATHER && !PAIR && !BLOCKW && MT == 1 && Elem<DT>::bytes == 2),
+  static_assert(!CONV || (!GATHER && !PAIR && MT == 1 && Elem<DT>::bytes == 2),
                 "convolution: 16-bit, 128-row tiles");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
   static_assert(KX == 1 || (KX == 2 && SPARSE && MT == 1 && !GATHER && !CONV && !BLOCKW),
@@ -195,20 +196,37 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
   ui.img = 0;
   ui.h0 = 0;
   if constexpr (C::CONVOLUTION) {
-    // units: 128-row blocks of C_out fastest, then pixel patches (image, row block)
-    const int32_t mb = u % p.MB, patch = u / p.MB;
+    int32_t mb, patch;
+    if constexpr (C::BLOCKWISE) {
+      // tile-wise filter: units are (schedule entry, pixel patch), entries (tiles by
+      // kept group count, longest first) outermost
+      const int32_t np = p.conv_nb * p.conv_patches;
+      const int32_t e = u / np;
+      patch = u - e * np;
+      const int32_t* sch = p.schedule + 4 * e;
+      const int32_t t = __ldg(sch + 0), L = __ldg(sch + 1), P = __ldg(sch + 2);
+      mb = t;
+      ui.nk = (L + C::BK - 1) / C::BK;    // kept (tap, 64-channel) groups
+      ui.a_row0 = 2 * P;                  // packed chunks of 128 rows, tile t from row 2 P
+      ui.idx_base = __ldg(p.offsets + t);
+      ui.L = L;
+    } else {
+      // units: 128-row blocks of C_out fastest, then pixel patches (image, row block)
+      mb = u % p.MB;
+      patch = u / p.MB;
+      ui.nk = p.nk;
+      ui.a_row0 = mb * 128;
+      ui.idx_base = 0;
+      ui.L = 0;
+    }
     ui.img = patch / p.conv_patches;
     ui.h0 = (patch - ui.img * p.conv_patches) * p.conv_rows;
     ui.phantom = false;
     ui.m0 = mb * 128;
     ui.n0 = (ui.img * p.conv_h + ui.h0) * p.conv_w;
     ui.ncols = min(p.conv_rows, p.conv_h - ui.h0) * p.conv_w;
-    ui.nk = p.nk;
-    ui.a_row0 = ui.m0;
     ui.meta_blk0 = mb * p.nk;
     ui.subs = 1;
-    ui.idx_base = 0;
-    ui.L = 0;
     return ui;
   }
   if constexpr (!GATHER) {
@@ -494,8 +512,10 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           if constexpr (CONV) {
             // tap (r, s) and 64 input channels of K stage kb, for the patch's image rows
             // shifted by the tap (out-of-range rows and columns read as zeros)
+            // (tile-wise filter: the kb-th kept (tap, 64-channel) group of the tile)
             const int32_t cblocks = p.conv_cin / 64;
-            const int32_t tap = kb / cblocks, c0 = (kb - tap * cblocks) * 64;
+            const int32_t g = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) : kb;
+            const int32_t tap = g / cblocks, c0 = (g - tap * cblocks) * 64;
             const int32_t r = tap / 3, sx = tap - 3 * r;
             ptx::tma_load_4d(sB, &tmB, &full[stage], c0, sx - 1, ui.h0 + r - 1, ui.img, pol_b);
           } else if constexpr (!GATHER) {
@@ -948,7 +968,9 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     // A as for the 2:4 / dense GEMM over the flattened filter; X as NHWC boxes of
     // BN / W whole image rows
     conv_rows = static_cast<int32_t>(BN / a.conv_w);
-    if constexpr (SPARSE)
+    if constexpr (BLOCKW)  // tile-wise filter: the packed kept groups seen as (packed_rows x 64)
+      ok = make_map(&tA, a.A, eb, 64, a.packed_rows, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    else if constexpr (SPARSE)
       ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, C::BM,
                     CU_TENSOR_MAP_SWIZZLE_64B);
     else
@@ -1048,7 +1070,8 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     p.conv_rows = conv_rows;
     p.conv_patches = static_cast<int32_t>(ceil_div(a.conv_h, conv_rows));
     p.conv_box_bytes = static_cast<uint32_t>(128 * conv_rows * a.conv_w);
-    p.num_units = p.MB * static_cast<int32_t>(a.conv_nb) * p.conv_patches;
+    p.conv_nb = static_cast<int32_t>(a.conv_nb);
+    p.num_units = (BLOCKW ? static_cast<int32_t>(a.nt) : p.MB) * p.conv_nb * p.conv_patches;
   }
   p.out_dt = a.out_dt == SSDNN_BF16 ? 1 : (a.out_dt == SSDNN_E4M3 ? 2 : 0);
   p.act = a.act;
@@ -1195,12 +1218,15 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
     }
     return sparse ? run<DT, true, false, 256>(a, s, err) : run<DT, false, false, 256>(a, s, err);
   }
-  if (mode == 5 || mode == 6) {
+  if (mode == 5 || mode == 6 || mode == 7) {
     // 3x3 convolution: N tiles of whole image rows, 224 columns (128 when that leaves
     // fewer than two tiles per SM)
     if constexpr (EB == 2) {
       const int64_t units224 = ceil_div(a.M, 128) * a.conv_nb * ceil_div(a.conv_h, 224 / a.conv_w);
       const bool narrow_c = a.conv_w <= 128 && units224 < 2 * sm_count();
+      if (mode == 7)  // tile-wise filter
+        return narrow_c ? run<DT, false, false, 128, 1, 128, false, true, true>(a, s, err)
+                        : run<DT, false, false, 224, 1, 128, false, true, true>(a, s, err);
       if (mode == 5)
         return narrow_c ? run<DT, true, false, 128, 1, 128, false, false, true>(a, s, err)
                         : run<DT, true, false, 224, 1, 128, false, false, true>(a, s, err);

@@ -45,7 +45,8 @@ bool gemm_variant_ok(int variant, bool sparse, int elem_bytes);
 
 // mode: 0 dense, 1 sp24, 2 TW (dense packed + gather), 3 TVW (2:4 packed + gather),
 // 4 block-wise (dense packed blocks, X panels by TMA), 5 / 6 3x3 convolution with a
-// 2:4 / dense filter (activation taps by 4-D TMA boxes of NHWC X)
+// 2:4 / dense filter (activation taps by 4-D TMA boxes of NHWC X), 7 3x3 convolution
+// with a tile-wise filter (the packed kept (tap, 64-channel) groups of each tile)
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* err);
 
 // Y = round(y_scale * act(bias[row])) for every element (the fused epilogue of a

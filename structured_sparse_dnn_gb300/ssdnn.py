@@ -69,6 +69,8 @@ _SIGS = {
                       _ptr], C.c_int),
     "dense_conv3x3": ([C.c_int, C.c_int, _i64, _i64, _i64, _i64, _i64, _ptr, _i64, _ptr, _ptr, _i64, C.c_float,
                        _ptr], C.c_int),
+    "tw_conv3x3": ([C.c_int, C.c_int, _i64, _i64, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64,
+                    C.c_float, _ptr], C.c_int),
     "tw_sizes": ([C.c_int, C.c_int, _i64, _i64, _i32p, C.POINTER(_sz), C.POINTER(_sz), C.POINTER(_sz),
                   C.POINTER(_sz), C.POINTER(_sz)], C.c_int),
     "tw_prune_compress": ([C.c_int, C.c_int, _ptr, _i64, _i64, _i64, _i32p, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
@@ -464,14 +466,22 @@ def ew_spmm(form: ElementWise, X: torch.Tensor, out: torch.Tensor | None = None)
 # ---------------------------------------------------------------- 3x3 convolution
 def conv3x3(filt, X: torch.Tensor, out: torch.Tensor | None = None, alpha: float = 1.0) -> torch.Tensor:
     """3x3 convolution (stride 1, zero padding 1) of NHWC activations X (Nb, H, W, Cin).
-    `filt` is either an Sp24 (the 2:4 form of the Cout x 9 Cin flattened filter) or
-    the dense flattened filter tensor. Returns Y as Cout x (Nb H W)."""
+    `filt` is an Sp24 (the 2:4 form of the Cout x 9 Cin flattened filter), a
+    BlockWise (the tile-wise filter: bw_prune_compress of the flattened filter, whose
+    64-column blocks are (tap, 64-channel) groups), or the dense flattened filter
+    tensor. Returns Y as Cout x (Nb H W)."""
     Nb, H, W, Cin = X.shape
     assert X.is_contiguous()
     dt = _DT[X.dtype]
-    Cout = filt.M if isinstance(filt, Sp24) else filt.shape[0]
+    Cout = filt.M if isinstance(filt, (Sp24, BlockWise)) else filt.shape[0]
     if out is None:
         out = torch.empty((Cout, Nb * H * W), dtype=X.dtype, device=X.device)
+    if isinstance(filt, BlockWise):
+        assert filt.K == 9 * Cin and filt.dt == dt
+        _check(lib.tw_conv3x3(dt, _DT[out.dtype], Cout, Cin, Nb, H, W, _kp(filt.keep), _p(filt.offsets),
+                              _p(filt.indices), _p(filt.schedule), _p(filt.packed), _p(X), _p(out), out.stride(0),
+                              alpha, _stream(X.device)), "tw_conv3x3")
+        return out
     if isinstance(filt, Sp24):
         assert filt.K == 9 * Cin and filt.dt == dt
         _check(lib.sp24_conv3x3(dt, _DT[out.dtype], Cout, Cin, Nb, H, W, _p(filt.values), _p(filt.meta_hw), _p(X),

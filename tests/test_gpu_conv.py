@@ -38,3 +38,36 @@ def test_conv3x3(dt, case, sparse):
     ok = oracle.gemm.within_bound(bits_of(Y), Y_ref, B, dt, REL[dt])
     assert ok.all(), f"{(~ok).sum()} of {ok.size} outside the bound"
     assert canary_intact(buf, Cout, N)
+
+
+# (Nb, H, W, Cin, Cout, kept groups per 128-channel tile); a group is one tap x 64
+# input channels, 9 Cin / 64 groups per tile
+TW_CASES = [(1, 5, 7, 64, 128, [3]), (2, 14, 14, 128, 256, [5, 0]), (1, 28, 28, 64, 200, [9, 2]),
+            (3, 9, 30, 64, 64, [1]), (1, 3, 224, 128, 128, [18])]
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("case", TW_CASES)
+def test_conv3x3_tile_wise_filter(dt, case):
+    """The tile-wise filter: bw_prune_compress of the flattened filter (indices and
+    packed operand bit-exact against the oracle) and tw_conv3x3 within the bound of
+    the oracle's convolution with the masked filter; a tile that keeps no group
+    writes zeros, a tile that keeps all groups is the dense convolution."""
+    ss = lib()
+    Nb, H, W, Cin, Cout, keep = case
+    keep = np.array(keep, dtype=np.int32)
+    X = rand_bits(1200 + H + W, (Nb * H * W, Cin), dt, 1.0).reshape(Nb, H, W, Cin)
+    Wf = rand_bits(1210 + Cout + Cin, (Cout, 9 * Cin), dt, 0.2)
+    Xd = dev_tensor(X.reshape(-1, Cin), dt).reshape(Nb, H, W, Cin)
+    N = Nb * H * W
+    pad = 8 + (-N) % 8
+    Y, buf = guarded_output(Cout, N, torch.bfloat16 if dt == "bf16" else torch.float16, pad_cols=pad)
+    f = ss.bw_prune_compress(dev_tensor(Wf, dt), keep)
+    ss.conv3x3(f, Xd, out=Y)
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
+    Y_ref, B, form = oracle.conv.conv3x3_tw(Wf, X, dt, dt, keep)
+    assert np.array_equal(f.indices.cpu().numpy()[:int(keep.sum())], form["indices"])
+    ok = oracle.gemm.within_bound(bits_of(Y), Y_ref, B, dt, REL[dt])
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outside the bound"
+    assert canary_intact(buf, Cout, N)
