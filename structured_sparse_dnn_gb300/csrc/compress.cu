@@ -10,108 +10,189 @@
 // or 32 B of e4m3 read with 16-byte loads, 32 B / 16 B of values and 4 B of
 // canonical metadata written, plus the word of the tensor-core operand layout of
 // the metadata. The grid also covers the 128-row and K-block padding of that
-// layout, which it fills with the (0,1) pattern.
+// layout, which it fills with the (0,1) pattern. A group's kept pair comes from six
+// pairwise magnitude comparisons made in parallel on the group's packed bytes
+// (e4m3) or 16-bit lanes, looked up in a 64-entry table of kept pairs.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace ssdnn {
 namespace {
 
-template <int EB>
-__device__ __forceinline__ uint32_t elem(const uint32_t (&w)[16], int j) {
-  if constexpr (EB == 2) {
-    return (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-  } else {
-    return (w[j >> 2] >> ((j & 3) * 8)) & 0xFFu;
-  }
+// The order of a group's four magnitudes m0..m3 as six comparison bits:
+//   b0 = [m0 >= m1]  b1 = [m1 >= m2]  b2 = [m2 >= m3]  b3 = [m3 > m0]
+//   b4 = [m0 >= m2]  b5 = [m1 >= m3]
+// (ties count for the lower position; the pair (3, 0) is compared strictly for that
+// reason). Entry idx of the shared table is, for the group's kept pair j0 < j1: the
+// metadata nibble j0 | j1 << 2 in bits 0..3, the byte selector of the pair within its
+// own word(s) in bits 8..23, and (e4m3) the selector of the pair as the high half of
+// a two-group output word in bits 24..31.
+__device__ __forceinline__ uint32_t kept_pair_entry(uint32_t idx, int eb) {
+  const uint32_t w01 = idx & 1u, w12 = (idx >> 1) & 1u, w23 = (idx >> 2) & 1u, w03 = 1u - ((idx >> 3) & 1u),
+                 w02 = (idx >> 4) & 1u, w13 = (idx >> 5) & 1u;
+  const uint32_t wins[4] = {w01 + w02 + w03, (1u - w01) + w12 + w13, (1u - w02) + (1u - w12) + w23,
+                            (1u - w03) + (1u - w13) + (1u - w23)};
+  // the two positions with the most wins, ties to the lower position
+  uint32_t a = 0;
+  for (uint32_t i = 1; i < 4; ++i)
+    if (wins[i] > wins[a]) a = i;
+  uint32_t b = a == 0 ? 1u : 0u;
+  for (uint32_t i = 0; i < 4; ++i)
+    if (i != a && wins[i] > wins[b]) b = i;
+  const uint32_t j0 = min(a, b), j1 = max(a, b);
+  const uint32_t nib = j0 | (j1 << 2);
+  if (eb == 1) return nib | ((j0 | (j1 << 4)) << 8) | (((j0 + 4) | ((j1 + 4) << 4)) << 24);
+  return nib | (((2 * j0) | ((2 * j0 + 1) << 4) | ((2 * j1) << 8) | ((2 * j1 + 1) << 12)) << 8);
 }
 
-// Block = 16 rows x 16 chunks (a warp reads 1 KB / 512 B contiguous of each of
-// two rows); grid.y walks 16-row groups of the 128-row-padded matrix.
+// The six order bits of a group of four e4m3 codes in one word (byte i = code i):
+// byte-parallel subtractions with a guard bit (magnitudes are 7 bits).
+__device__ __forceinline__ uint32_t order_bits_e4m3(uint32_t w) {
+  const uint32_t m = w & 0x7F7F7F7Fu;
+  const uint32_t mo = m | 0x80808080u;
+  const uint32_t r1 = __byte_perm(m, 0u, 0x0321);  // byte i: m_{(i+1) % 4}
+  const uint32_t r2 = __byte_perm(m, 0u, 0x1032);  // byte i: m_{(i+2) % 4}
+  // bit 7 of byte i: [m_i >= m_{i+1}] (byte 3 strict: [m_3 > m_0]); bits 7, 15: [m0 >= m2], [m1 >= m3]
+  const uint32_t ge1 = (mo - r1 - 0x01000000u) & 0x80808080u;
+  const uint32_t ge2 = (mo - r2) & 0x00008080u;
+  // gather bits 7, 15, 23, 31 of ge1 and 7, 15 of ge2 into bits 24..29
+  const uint32_t z = (ge1 >> 7) | (ge2 >> 3);
+  return (z * 0x01020408u) >> 24;
+}
+
+// The same for a group of four 16-bit codes in two words (lo = v0 | v1 << 16,
+// hi = v2 | v3 << 16): lane-parallel subtractions with a guard bit (15-bit magnitudes).
+__device__ __forceinline__ uint32_t order_bits_16(uint32_t lo, uint32_t hi) {
+  const uint32_t ml = lo & 0x7FFF7FFFu, mh = hi & 0x7FFF7FFFu;
+  const uint32_t gl = ml | 0x80008000u, gh = mh | 0x80008000u;
+  const uint32_t da = gl - __byte_perm(ml, 0u, 0x1032);  // bit 15: [m0 >= m1]
+  const uint32_t db = gh - __byte_perm(mh, 0u, 0x1032);  // bit 15: [m2 >= m3]
+  const uint32_t dc = gl - mh;                           // bits 15, 31: [m0 >= m2], [m1 >= m3]
+  // lanes (m1, m3) against (m2, m0), the upper lane strictly: bits 15, 31: [m1 >= m2], [m3 > m0]
+  const uint32_t x = __byte_perm(ml, mh, 0x7632) | 0x80008000u;
+  const uint32_t y = __byte_perm(mh, ml, 0x5410);
+  const uint32_t dd = x - y - 0x00010000u;
+  // b0, b1, b2, b3 to bits 7, 15, 23, 31 (bytes da.1, dd.1, db.1, dd.3) and b4, b5 to
+  // bits 7, 15 (bytes dc.1, dc.3), then gathered as for e4m3
+  const uint32_t v = (__byte_perm(da, dd, 0x7051) & 0x80008080u) | ((db << 8) & 0x00800000u);
+  const uint32_t u = __byte_perm(dc, 0u, 0x0031) & 0x00008080u;
+  const uint32_t z = (v >> 7) | (u >> 3);
+  return (z * 0x01020408u) >> 24;
+}
+
+// A thread owns CPT chunks of 32 consecutive elements of a row (8 groups each):
+// 64 B (fp16/bf16, one chunk) or 2 x 32 B (e4m3, two adjacent chunks), all loaded
+// before any is processed; block = 16 rows x 16 threads; grid.y walks 16-row
+// groups of the 128-row-padded matrix.
 template <int EB>
 __global__ void __launch_bounds__(256) k_sp24_compress(const uint8_t* __restrict__ W, int64_t M, int64_t K,
                                                        int64_t ldw_b, uint8_t* __restrict__ values,
                                                        int64_t ldv_b, uint8_t* __restrict__ meta, int64_t ldm,
                                                        uint8_t* __restrict__ meta_hw, int64_t KBhw,
                                                        int64_t chunks_pad, bool vec_ok) {
-  constexpr uint32_t kMask = (EB == 2) ? 0x7FFFu : 0x7Fu;
+  constexpr int CPT = EB == 1 ? 2 : 1;  // chunks per thread
   __shared__ uint32_t s_nib[16][17];
+  __shared__ uint32_t s_tab[64];
   const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
   const int64_t i = static_cast<int64_t>(blockIdx.y) * 16 + tr;
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * 16 + tc;
-  const int64_t k0 = c * 32;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 16 + tc) * CPT;  // first chunk
   const int64_t Kp = (K + 31) / 32 * 32;
 
-  uint32_t nib = 0x44444444u;
-  uint32_t outv[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 16 values packed (EB bytes each)
-  if (i < M && k0 < K) {
-    uint32_t w[16];
+  uint32_t w[CPT][16];
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) {
+    const int64_t k0 = (c0 + cc) * 32;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) w[cc][q] = 0;
+    if (i >= M || k0 >= K) continue;
     const uint8_t* src = W + i * ldw_b + k0 * EB;
     if (vec_ok && k0 + 32 <= K) {
 #pragma unroll
       for (int q = 0; q < 2 * EB; ++q) {  // 32 elements = 2 * EB 16-byte loads
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + q);
-        w[4 * q + 0] = v.x;
-        w[4 * q + 1] = v.y;
-        w[4 * q + 2] = v.z;
-        w[4 * q + 3] = v.w;
-      }
-      if constexpr (EB == 1) {
-#pragma unroll
-        for (int q = 8; q < 16; ++q) w[q] = 0;
+        w[cc][4 * q + 0] = v.x;
+        w[cc][4 * q + 1] = v.y;
+        w[cc][4 * q + 2] = v.z;
+        w[cc][4 * q + 3] = v.w;
       }
     } else {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) w[q] = 0;
-#pragma unroll
       for (int j = 0; j < 32; ++j) {
         if (k0 + j >= K) break;
-        uint32_t e = (EB == 2) ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(src)[j])
-                               : static_cast<uint32_t>(src[j]);
+        const uint32_t e = (EB == 2) ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(src)[j])
+                                     : static_cast<uint32_t>(src[j]);
         if constexpr (EB == 2)
-          w[j >> 1] |= e << ((j & 1) * 16);
+          w[cc][j >> 1] |= e << ((j & 1) * 16);
         else
-          w[j >> 2] |= e << ((j & 3) * 8);
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      if (k0 + 4 * g + 4 > K) break;  // K % 4 == 0: a group is entirely in or out
-      const uint32_t e0 = elem<EB>(w, 4 * g + 0), e1 = elem<EB>(w, 4 * g + 1);
-      const uint32_t e2 = elem<EB>(w, 4 * g + 2), e3 = elem<EB>(w, 4 * g + 3);
-      const uint32_t sel = top2_nibble(e0 & kMask, e1 & kMask, e2 & kMask, e3 & kMask);
-      const uint32_t j0 = sel & 3u, j1 = sel >> 2;
-      nib = (nib & ~(0xFu << (4 * g))) | (sel << (4 * g));
-      // gather the two kept values with one byte permute of the group's bytes
-      if constexpr (EB == 2) {
-        outv[g] = __byte_perm(w[2 * g], w[2 * g + 1],
-                              (2 * j0) | ((2 * j0 + 1) << 4) | ((2 * j1) << 8) | ((2 * j1 + 1) << 12));
-      } else {
-        outv[g >> 1] |= __byte_perm(w[g], 0u, j0 | (j1 << 4) | 0x4400u) << ((g & 1) * 16);
+          w[cc][j >> 2] |= e << ((j & 3) * 8);
       }
     }
   }
-  if (i < M && k0 < Kp) {
-    uint8_t* dv = values + i * ldv_b + c * 16 * EB;
-    reinterpret_cast<uint4*>(dv)[0] = make_uint4(outv[0], outv[1], outv[2], outv[3]);
-    if constexpr (EB == 2) reinterpret_cast<uint4*>(dv)[1] = make_uint4(outv[4], outv[5], outv[6], outv[7]);
-    if (meta) *reinterpret_cast<uint32_t*>(meta + i * ldm + c * 4) = nib;
+
+  // the kept-pair table, built while the loads are in flight
+  if (threadIdx.x < 64) s_tab[threadIdx.x] = kept_pair_entry(threadIdx.x, EB);
+  __syncthreads();
+
+  uint32_t nib[CPT];
+  uint32_t outv[CPT][8];  // 16 kept values (EB bytes each) per chunk
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) {
+    const int64_t k0 = (c0 + cc) * 32;
+    // groups past K (K % 4 == 0: a group is entirely in or out) take the (0, 1)
+    // entry: nibble 0x4, the zero values loaded there
+    const int ngroups = (i >= M || k0 >= K) ? 0 : ((K - k0) / 4 < 8 ? static_cast<int>((K - k0) / 4) : 8);
+    uint32_t nw = 0;
+    if constexpr (EB == 1) {
+#pragma unroll
+      for (int g = 0; g < 8; g += 2) {
+        const uint32_t e0 = g < ngroups ? s_tab[order_bits_e4m3(w[cc][g])] : 0x54001004u;
+        const uint32_t e1 = g + 1 < ngroups ? s_tab[order_bits_e4m3(w[cc][g + 1])] : 0x54001004u;
+        nw |= ((e0 & 0xFu) | ((e1 & 0xFu) << 4)) << (4 * g);
+        const uint32_t sel = ((e0 >> 8) & 0xFFu) | ((e1 >> 16) & 0xFF00u);
+        outv[cc][g >> 1] = __byte_perm(w[cc][g], w[cc][g + 1], sel);
+      }
+#pragma unroll
+      for (int q = 4; q < 8; ++q) outv[cc][q] = 0u;
+    } else {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t e = g < ngroups ? s_tab[order_bits_16(w[cc][2 * g], w[cc][2 * g + 1])] : 0x321004u;
+        nw |= (e & 0xFu) << (4 * g);
+        outv[cc][g] = __byte_perm(w[cc][2 * g], w[cc][2 * g + 1], e >> 8);
+      }
+    }
+    nib[cc] = nw;
+  }
+  if (i < M) {
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) {
+      const int64_t c = c0 + cc;
+      if (c * 32 >= Kp) break;
+      uint8_t* dv = values + i * ldv_b + c * 16 * EB;
+      reinterpret_cast<uint4*>(dv)[0] = make_uint4(outv[cc][0], outv[cc][1], outv[cc][2], outv[cc][3]);
+      if constexpr (EB == 2)
+        reinterpret_cast<uint4*>(dv)[1] = make_uint4(outv[cc][4], outv[cc][5], outv[cc][6], outv[cc][7]);
+      if (meta) *reinterpret_cast<uint32_t*>(meta + i * ldm + c * 4) = nib[cc];
+    }
   }
   const int64_t mb = i >> 7, r = i & 127;
   if constexpr (EB == 1) {
     // e4m3 operand order = canonical nibbles, 16 bytes per row per 128 columns of K
-    if (c < chunks_pad)
-      *reinterpret_cast<uint32_t*>(meta_hw + ((mb * KBhw + (c >> 2)) * 128 + r) * 16 + (c & 3) * 4) = nib;
+    // (the thread's two chunks are adjacent: 8 bytes, one store)
+    if (c0 < chunks_pad)
+      *reinterpret_cast<uint2*>(meta_hw + ((mb * KBhw + (c0 >> 2)) * 128 + r) * 16 + (c0 & 3) * 4) =
+          make_uint2(nib[0], nib[1]);
   } else {
     // 16-bit operand order: rows r and r ^ 8 share one 32-bit word per 32-column
     // span (lower row: groups 0..3 of both rows; upper row: groups 4..7 of both),
     // each span in its own even TMEM column (odd words zero).
-    s_nib[tr][tc] = nib;
+    s_nib[tr][tc] = nib[0];
     __syncthreads();
     const uint32_t partner = s_nib[tr ^ 8][tc];
-    const uint32_t hw = (tr & 8) ? ((partner >> 16) | (nib & 0xFFFF0000u)) : ((nib & 0xFFFFu) | (partner << 16));
-    if (c < chunks_pad)
-      *reinterpret_cast<uint2*>(meta_hw + ((mb * KBhw + (c >> 1)) * 128 + r) * 16 + (c & 1) * 8) =
+    const uint32_t hw =
+        (tr & 8) ? ((partner >> 16) | (nib[0] & 0xFFFF0000u)) : ((nib[0] & 0xFFFFu) | (partner << 16));
+    if (c0 < chunks_pad)
+      *reinterpret_cast<uint2*>(meta_hw + ((mb * KBhw + (c0 >> 1)) * 128 + r) * 16 + (c0 & 1) * 8) =
           make_uint2(hw, 0u);
   }
 }
@@ -128,7 +209,8 @@ cudaError_t launch_sp24_compress(int dt, const void* W, int64_t M, int64_t K, in
   if (MB == 0 || KBhw == 0) return cudaSuccess;
   const int64_t Kp = round_up(K, 32);
   const bool vec_ok = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && ((ldw * EB) % 16 == 0);
-  const dim3 grid(static_cast<unsigned>(ceil_div(chunks_pad, 16)), static_cast<unsigned>(MB * 8));
+  const int64_t cpt = EB == 1 ? 2 : 1;  // chunks per thread (chunks_pad is a multiple of 4 for e4m3)
+  const dim3 grid(static_cast<unsigned>(ceil_div(chunks_pad, 16 * cpt)), static_cast<unsigned>(MB * 8));
   if (EB == 2)
     k_sp24_compress<2><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(W), M, K, ldw * 2,
                                             static_cast<uint8_t*>(values), Kp / 2 * 2, meta, Kp / 8, meta_hw, KBhw,
