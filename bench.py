@@ -581,16 +581,16 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
         groups = 9 * Cin // 64
         keep_g = np.full((Cout + 127) // 128, max(1, round(0.25 * groups)), dtype=np.int32)
         ft = ss.bw_prune_compress(Wc, keep_g)
-        t_tw = statistics.mean(timed_steps(lambda: ss.conv3x3(ft, Xc, out=Yc), steps, 2, flush, stream))
+        t_twc = statistics.mean(timed_steps(lambda: ss.conv3x3(ft, Xc, out=Yc), steps, 2, flush, stream))
         flops = 2.0 * Cout * 9 * Cin * Nb * H * H
         kept = float(keep_g[0]) / groups
         conv_rows[f"{H}x{H}x{Cin}->{Cout}, batch {Nb}"] = {
             "sp24_ms": round(t_sp, 4), "dense_ms": round(t_dn, 4),
             "sp24_effective_TFLOP/s": round(0.5 * flops / (t_sp * 1e-3) / 1e12, 1),
             "dense_TFLOP/s": round(flops / (t_dn * 1e-3) / 1e12, 1), "speedup": round(t_dn / t_sp, 3),
-            "tw_kept_fraction": round(kept, 4), "tw_ms": round(t_tw, 4),
-            "tw_effective_TFLOP/s": round(kept * flops / (t_tw * 1e-3) / 1e12, 1),
-            "tw_speedup": round(t_dn / t_tw, 3)}
+            "tw_kept_fraction": round(kept, 4), "tw_ms": round(t_twc, 4),
+            "tw_effective_TFLOP/s": round(kept * flops / (t_twc * 1e-3) / 1e12, 1),
+            "tw_speedup": round(t_dn / t_twc, 3)}
         del Xc, Wc, fc, ft, Yc
     rows["conv3x3_resnet50"] = conv_rows
     rows["tile_wise"] = {
