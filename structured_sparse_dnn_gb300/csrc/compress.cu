@@ -12,7 +12,8 @@
 // the metadata. The grid also covers the 128-row and K-block padding of that
 // layout, which it fills with the (0,1) pattern. A group's kept pair comes from six
 // pairwise magnitude comparisons made in parallel on the group's packed bytes
-// (e4m3) or 16-bit lanes, looked up in a 64-entry table of kept pairs.
+// (e4m3) or 16-bit lanes, looked up in a 64-entry table of kept pairs (e4m3: a byte
+// table of selectors, four groups' selectors combined in one word).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(256) k_sp24_compress(const uint8_t* __restrict
   constexpr int CPT = EB == 1 ? 2 : 1;  // chunks per thread
   __shared__ uint32_t s_nib[16][17];
   __shared__ uint32_t s_tab[64];
+  __shared__ uint8_t s_sel[64];  // e4m3: j0 | j1 << 4 of the kept pair (one byte: no bank conflicts)
   const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
   const int64_t i = static_cast<int64_t>(blockIdx.y) * 16 + tr;
   const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 16 + tc) * CPT;  // first chunk
@@ -130,7 +132,11 @@ __global__ void __launch_bounds__(256) k_sp24_compress(const uint8_t* __restrict
   }
 
   // the kept-pair table, built while the loads are in flight
-  if (threadIdx.x < 64) s_tab[threadIdx.x] = kept_pair_entry(threadIdx.x, EB);
+  if (threadIdx.x < 64) {
+    const uint32_t e = kept_pair_entry(threadIdx.x, EB);
+    s_tab[threadIdx.x] = e;
+    s_sel[threadIdx.x] = static_cast<uint8_t>(e >> 8);
+  }
   __syncthreads();
 
   uint32_t nib[CPT];
@@ -143,16 +149,31 @@ __global__ void __launch_bounds__(256) k_sp24_compress(const uint8_t* __restrict
     const int ngroups = (i >= M || k0 >= K) ? 0 : ((K - k0) / 4 < 8 ? static_cast<int>((K - k0) / 4) : 8);
     uint32_t nw = 0;
     if constexpr (EB == 1) {
+      // the groups' selector bytes j0 | j1 << 4 (groups past K: (0, 1)), four to a word
+      uint32_t sb[8];
+      if (ngroups == 8) {
 #pragma unroll
-      for (int g = 0; g < 8; g += 2) {
-        const uint32_t e0 = g < ngroups ? s_tab[order_bits_e4m3(w[cc][g])] : 0x54001004u;
-        const uint32_t e1 = g + 1 < ngroups ? s_tab[order_bits_e4m3(w[cc][g + 1])] : 0x54001004u;
-        nw |= ((e0 & 0xFu) | ((e1 & 0xFu) << 4)) << (4 * g);
-        const uint32_t sel = ((e0 >> 8) & 0xFFu) | ((e1 >> 16) & 0xFF00u);
-        outv[cc][g >> 1] = __byte_perm(w[cc][g], w[cc][g + 1], sel);
+        for (int g = 0; g < 8; ++g) sb[g] = s_sel[order_bits_e4m3(w[cc][g])];
+      } else {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) sb[g] = g < ngroups ? s_sel[order_bits_e4m3(w[cc][g])] : 0x10u;
       }
+      const uint32_t S0 = __byte_perm(__byte_perm(sb[0], sb[1], 0x0040), __byte_perm(sb[2], sb[3], 0x0040), 0x5410);
+      const uint32_t S1 = __byte_perm(__byte_perm(sb[4], sb[5], 0x0040), __byte_perm(sb[6], sb[7], 0x0040), 0x5410);
+      // output word of groups (g, g + 1): selector j0 | j1 << 4 | (j0' + 4) << 8 | (j1' + 4) << 12
+      outv[cc][0] = __byte_perm(w[cc][0], w[cc][1], S0 + 0x4400u);
+      outv[cc][1] = __byte_perm(w[cc][2], w[cc][3], (S0 >> 16) + 0x4400u);
+      outv[cc][2] = __byte_perm(w[cc][4], w[cc][5], S1 + 0x4400u);
+      outv[cc][3] = __byte_perm(w[cc][6], w[cc][7], (S1 >> 16) + 0x4400u);
 #pragma unroll
       for (int q = 4; q < 8; ++q) outv[cc][q] = 0u;
+      // nibble j0 | j1 << 2 of each selector byte, then the bytes' nibbles packed in order
+      auto nibbles = [](uint32_t S) {
+        const uint32_t n = (S | (S >> 2)) & 0x0F0F0F0Fu;
+        const uint32_t t = (n | (n >> 4)) & 0x00FF00FFu;
+        return (t | (t >> 8)) & 0xFFFFu;
+      };
+      nw = nibbles(S0) | (nibbles(S1) << 16);
     } else {
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
