@@ -776,13 +776,17 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
         }
         pack_row32(p.out_dt, x, w);
       };
-      // this warp's part of the accumulator has been read: release it
+      // this warp's part of the accumulator has been read (its tcgen05.ld have
+      // completed: tmem_ld_wait precedes every call): release it
       auto release = [&]() {
         ptx::tc_fence_before();
         if (leader)
           ptx::mbar_arrive(&acc_empty[acc]);
-        else  // the odd CTA of a pair releases its rows on the even CTA's barrier
-          ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&acc_empty[acc]), crank & ~1u));
+        else  // the odd CTA of a pair releases its rows on the even CTA's barrier. The
+              // arrive is relaxed: the reads it signals are complete, and a
+              // cluster-scope release would also wait for this thread's earlier
+              // stores (it cost the pair kernel about 0.4 us per tile)
+          ptx::mbar_arrive_cluster_relaxed(ptx::mapa(ptx::smem_u32(&acc_empty[acc]), crank & ~1u));
       };
       auto store_chunk = [&](int c, const uint32_t (&w)[16]) {
         const int32_t n0 = ui.n0 + 32 * c;
