@@ -52,17 +52,20 @@ def peaks() -> dict:
 
 def measured_traffic(workload: str):
     """DRAM bytes (read + write) per launch of the sparse GEMM on this workload from
-    the committed ncu capture, if the kernel source is unchanged since; else None."""
+    the committed ncu capture, if the kernel's sources (gemm.cu, ptx.cuh, common.cuh)
+    are unchanged since; else None."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         tab = json.load(f)
-    with open(os.path.join(ROOT, "structured_sparse_dnn_gb300", "csrc", "gemm.cu"), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "structured_sparse_dnn_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     ent = tab.get(workload)
-    if not ent or ent.get("gemm_cu_sha256_16") != sha:
+    if not ent or ent.get("kernel_src_sha256_16") != h.hexdigest()[:16]:
         return None
     return ent["dram_bytes_per_launch"]
 
