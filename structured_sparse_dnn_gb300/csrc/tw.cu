@@ -9,18 +9,20 @@
 // ascending), listed ascending; TVW groups are four consecutive kept columns.
 //
 // Three kernels:
-//   k_tw_score   one thread per (tile, 8 consecutive k): walks the tile's rows
-//                with 16-byte loads (coalesced across threads), fp32 sums in row
-//                order, writes scores to the caller's workspace.
+//   k_tw_score   one CTA per (tile, 128 consecutive k): stages the tile's 128 x
+//                128 block in shared memory with coalesced 16-byte loads, then one
+//                thread per k sums the rows in order (fp32), into the caller's
+//                workspace.
 //   k_tw_select  one CTA per tile: exact top-L by a 4-pass 8-bit radix select on
-//                the score bits (non-negative floats order like their bits), then
-//                an ascending-k compaction with block prefix sums that takes ties
-//                at the threshold from the lowest k.
-//   k_tw_pack    one warp per (tile, 64-column chunk, row), 16 rows per CTA:
-//                gathers the kept columns of the row into the chunk-blocked packed
-//                operand; TVW selects 2 of every 4 and writes values plus metadata
-//                in the canonical and the tensor-core operand order (which pairs
-//                rows r and r ^ 8, exchanged through shared memory).
+//                the score bits (non-negative floats order like their bits; each
+//                pass's digit found by one warp's scan of the histogram), then an
+//                ascending-k compaction with one block prefix sum per 1024 keys
+//                that takes ties at the threshold from the lowest k.
+//   k_tw_pack    one warp per (row or TVW row pair, four 64-column chunks of a
+//                tile): gathers the kept columns of the row into the chunk-blocked
+//                packed operand; TVW selects 2 of every 4 and writes values plus
+//                metadata in the canonical and the tensor-core operand order (which
+//                pairs rows r and r ^ 8, the two halves of one warp).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -39,42 +41,55 @@ __device__ __forceinline__ float mag16(uint32_t h) {
   }
 }
 
+// One CTA per (tile, 128 consecutive k): the tile's 128 rows x 128 columns (32 KB)
+// are loaded with coalesced 16-byte loads into shared memory, then thread j sums
+// column j over the rows in ascending order.
 template <int DT>
-__global__ void __launch_bounds__(256) k_tw_score(const uint8_t* __restrict__ W, int64_t M, int64_t K,
+__global__ void __launch_bounds__(128) k_tw_score(const uint8_t* __restrict__ W, int64_t M, int64_t K,
                                                   int64_t ldw_b, float* __restrict__ scores, bool vec_ok) {
+  __shared__ __align__(16) uint16_t s_w[128][128];
   const int64_t t = blockIdx.y;
-  const int64_t k0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-  if (k0 >= K) return;
+  const int64_t kb = static_cast<int64_t>(blockIdx.x) * 128;
   const int64_t r0 = t * 128;
-  const int64_t r1 = min(M, r0 + 128);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (vec_ok && k0 + 8 <= K) {
-    const uint8_t* p = W + r0 * ldw_b + k0 * 2;
-#pragma unroll 8
-    for (int64_t i = r0; i < r1; ++i, p += ldw_b) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const int rows = static_cast<int>(M - r0 < 128 ? M - r0 : 128);
+  // 16-byte segment `seg` of rows rsub, rsub + 8, ...: 16 threads cover a row's 256 bytes
+  const int seg = static_cast<int>(threadIdx.x & 15u), rsub = static_cast<int>(threadIdx.x >> 4);
+  const int64_t kseg = kb + 8 * seg;
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint4 v[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[2 * j] = acc[2 * j] + mag16<DT>(w[j] & 0xFFFFu);
-        acc[2 * j + 1] = acc[2 * j + 1] + mag16<DT>(w[j] >> 16);
+    for (int i = 0; i < 8; ++i) {
+      const int r = rsub + 8 * (8 * half + i);
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) {
+        const uint8_t* p = W + (r0 + r) * ldw_b + kseg * 2;
+        if (vec_ok && kseg + 8 <= K) {
+          v[i] = __ldg(reinterpret_cast<const uint4*>(p));
+        } else {
+          uint32_t e[4] = {0u, 0u, 0u, 0u};
+          for (int j = 0; j < 8; ++j)
+            if (kseg + j < K) e[j >> 1] |= static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(p)[j]) << (16 * (j & 1));
+          v[i] = make_uint4(e[0], e[1], e[2], e[3]);
+        }
       }
     }
-  } else {
-    for (int64_t i = r0; i < r1; ++i) {
-      const uint16_t* p = reinterpret_cast<const uint16_t*>(W + i * ldw_b) + k0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (k0 + j < K) acc[j] = acc[j] + mag16<DT>(p[j]);
-    }
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<uint4*>(&s_w[rsub + 8 * (8 * half + i)][8 * seg]) = v[i];
   }
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (k0 + j < K) scores[t * K + k0 + j] = acc[j];
+  __syncthreads();
+  const int64_t k = kb + threadIdx.x;
+  if (k >= K) return;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int r = 0; r < rows; ++r) acc = acc + mag16<DT>(s_w[r][threadIdx.x]);
+  scores[t * K + k] = acc;
 }
 
-// Exclusive prefix sum over a 1024-thread block; returns this thread's prefix and
-// writes the block total to *total. `ws` holds 32 words of shared scratch.
+// Exclusive prefix sum over the block (whole warps, at most 1024 threads); returns
+// this thread's prefix and writes the block total to *total. `ws` holds 32 words of
+// shared scratch.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* ws, uint32_t* total) {
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -101,7 +116,10 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* ws, ui
   return warp_prefix + x - v;
 }
 
-__global__ void __launch_bounds__(1024) k_tw_select(const float* __restrict__ scores, int64_t K,
+// NT threads per CTA: 1024 for the few tiles of a tile-wise weight (the CTA's latency
+// is the kernel's), 256 for the many rows of the element-wise prune (more CTAs per SM).
+template <int NT>
+__global__ void __launch_bounds__(NT) k_tw_select(const float* __restrict__ scores, int64_t K,
                                                     const int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ indices) {
   __shared__ uint32_t hist[256];
@@ -116,112 +134,167 @@ __global__ void __launch_bounds__(1024) k_tw_select(const float* __restrict__ sc
   uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(L);
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
     __syncthreads();
     for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
       const uint32_t x = key[k];
       if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t cum = 0;
-      for (int d = 255; d >= 0; --d) {
-        const uint32_t h = hist[d];
-        if (cum + h >= remaining) {
-          s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
-          s_remaining = remaining - cum;
-          break;
+    if (threadIdx.x < 32) {
+      // the digit whose keys, counted from the largest digit down, reach `remaining`:
+      // lane l sums bins 255 - 8 l .. 248 - 8 l, a warp scan orders the lanes, and
+      // the first lane whose running count reaches `remaining` walks its eight bins
+      const uint32_t lane = threadIdx.x;
+      uint32_t h[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        h[i] = hist[255u - 8u * lane - static_cast<uint32_t>(i)];
+        sum += h[i];
+      }
+      uint32_t inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= static_cast<uint32_t>(o)) inc += y;
+      }
+      const uint32_t found = __ballot_sync(0xffffffffu, inc >= remaining);
+      if (found == 0u) {  // L > K (refused by the host): take every key
+        if (lane == 0) {
+          s_prefix = 0u;
+          s_remaining = 0u;
         }
-        cum += h;
+      } else if (lane == static_cast<uint32_t>(__ffs(found) - 1)) {
+        uint32_t cum = inc - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + h[i] >= remaining) {
+            s_prefix = prefix | ((255u - 8u * lane - static_cast<uint32_t>(i)) << shift);
+            s_remaining = remaining - cum;
+            break;
+          }
+          cum += h[i];
+        }
       }
     }
     __syncthreads();
     prefix = s_prefix;
     remaining = s_remaining;
     mask |= 255u << shift;
-    __syncthreads();
   }
   // prefix = the L-th largest key; take every key above it and the `remaining`
-  // lowest-k keys equal to it.
+  // lowest-k keys equal to it. A taken key's place is the number of larger keys
+  // before it plus the number of equal keys before it (at most `remaining`): one
+  // block scan of both counts (16 bits each) per 1024 keys.
   const uint32_t thr = prefix, take_eq = remaining;
-  uint32_t base = 0, eq_base = 0;
+  uint32_t gt_base = 0, eq_base = 0;
   for (int64_t k0 = 0; k0 < K; k0 += blockDim.x) {
     const int64_t k = k0 + threadIdx.x;
     const uint32_t x = (k < K) ? key[k] : 0u;
     const uint32_t gt = (k < K && x > thr) ? 1u : 0u;
     const uint32_t eq = (k < K && x == thr) ? 1u : 0u;
-    uint32_t eq_total, take_total;
-    const uint32_t eq_rank = eq_base + block_excl_scan(eq, ws, &eq_total);
-    const uint32_t take = gt | ((eq && eq_rank < take_eq) ? 1u : 0u);
-    const uint32_t pos = base + block_excl_scan(take, ws, &take_total);
-    if (take) out[pos] = static_cast<int32_t>(k);
-    base += take_total;
-    eq_base += eq_total;
+    uint32_t total;
+    const uint32_t ex = block_excl_scan(gt | (eq << 16), ws, &total);
+    const uint32_t gt_before = gt_base + (ex & 0xFFFFu), eq_before = eq_base + (ex >> 16);
+    const bool take = gt != 0u || (eq != 0u && eq_before < take_eq);
+    const uint32_t pos = gt_before + (eq_before < take_eq ? eq_before : take_eq);
+    if (take && pos < static_cast<uint32_t>(L)) out[pos] = static_cast<int32_t>(k);
+    gt_base += total & 0xFFFFu;
+    eq_base += total >> 16;
   }
 }
 
-// 512 threads = 16 warps = 16 consecutive rows of one 64-column chunk of a tile:
-// blockIdx.x = chunk * 8 + row group, blockIdx.y = schedule entry (t, L, P, Q).
+// 512 threads = 16 warps; blockIdx.y = schedule entry (t, L, P, Q), blockIdx.x = chunk
+// group * row groups + row group. Each warp packs kPackChunks consecutive 64-column
+// chunks, all index and weight loads of which are independent and issued together.
+// TW: warp w packs row 16 g + w. TVW: warp w packs rows r and r + 8 (lanes 0-15 and
+// 16-31, r = 32 g + 16 (w >> 3) + (w & 7)), so the pair of rows that share the
+// tensor-core metadata words meets inside one warp.
+constexpr int kPackChunks = 4;
 template <int DT, bool TVW>
 __global__ void __launch_bounds__(512) k_tw_pack(const uint8_t* __restrict__ W, int64_t M, int64_t ldw_b,
                                                  const int32_t* __restrict__ offsets,
                                                  const int32_t* __restrict__ indices,
                                                  const int32_t* __restrict__ schedule, uint16_t* __restrict__ packed,
                                                  uint8_t* __restrict__ meta, uint8_t* __restrict__ meta_hw) {
-  __shared__ uint32_t s_words[16][2];
+  constexpr int GROUPS = TVW ? 4 : 8;  // row groups per tile (32 or 16 rows each)
   const int32_t* e = schedule + 4 * blockIdx.y;
   const int64_t t = e[0], L = e[1], P = e[2], Q = e[3];
-  const int64_t R = (L + 63) / 64 * 64;
-  const int64_t c = blockIdx.x >> 3;
-  if (c * 64 >= R) return;  // uniform over the block
+  const int64_t nch = (L + 63) / 64;  // chunks of the tile
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x / GROUPS) * kPackChunks;
+  if (c0 >= nch) return;  // uniform over the block
+  const int g = static_cast<int>(blockIdx.x % GROUPS);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-  const int64_t r = 16 * (blockIdx.x & 7) + warp;
-  const int64_t row = t * 128 + r;
   const int32_t* idx = indices + offsets[t];
-  const uint16_t* wrow = reinterpret_cast<const uint16_t*>(W + (row < M ? row : 0) * ldw_b);
   if constexpr (!TVW) {
-    uint32_t v = 0;
+    const int64_t r = 16 * g + warp;
+    const int64_t row = t * 128 + r;
+    const uint16_t* wrow = reinterpret_cast<const uint16_t*>(W + (row < M ? row : 0) * ldw_b);
+    int32_t k[kPackChunks][2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t j = c * 64 + 2 * lane + h;
-      if (j < L && row < M) v |= static_cast<uint32_t>(wrow[idx[j]]) << (16 * h);
+    for (int cc = 0; cc < kPackChunks; ++cc)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t j = (c0 + cc) * 64 + 2 * lane + h;
+        k[cc][h] = (j < L && row < M) ? __ldg(idx + j) : -1;
+      }
+    uint32_t v[kPackChunks];
+#pragma unroll
+    for (int cc = 0; cc < kPackChunks; ++cc) {
+      v[cc] = 0u;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (k[cc][h] >= 0) v[cc] |= static_cast<uint32_t>(__ldg(wrow + k[cc][h])) << (16 * h);
     }
-    *reinterpret_cast<uint32_t*>(packed + 128 * P + 8192 * c + 64 * r + 2 * lane) = v;
+#pragma unroll
+    for (int cc = 0; cc < kPackChunks; ++cc)
+      if (c0 + cc < nch)
+        *reinterpret_cast<uint32_t*>(packed + 128 * P + 8192 * (c0 + cc) + 64 * r + 2 * lane) = v[cc];
   } else {
-    uint32_t nib = 0;
-    if (lane < 16) {
-      const int64_t j = c * 64 + 4 * lane;
-      uint32_t v01 = 0;
-      nib = 0x4u;
-      if (j < L && row < M) {  // L % 4 == 0: the group is entirely kept
-        const uint32_t e0 = wrow[idx[j]], e1 = wrow[idx[j + 1]], e2 = wrow[idx[j + 2]], e3 = wrow[idx[j + 3]];
-        nib = top2_nibble(e0 & 0x7FFFu, e1 & 0x7FFFu, e2 & 0x7FFFu, e3 & 0x7FFFu);
+    const uint32_t half = lane >> 4, hl = lane & 15u;
+    const int64_t r = 32 * g + 16 * (warp >> 3) + (warp & 7u) + 8 * half;
+    const int64_t row = t * 128 + r;
+    const uint16_t* wrow = reinterpret_cast<const uint16_t*>(W + (row < M ? row : 0) * ldw_b);
+    int32_t k[kPackChunks][4];
+#pragma unroll
+    for (int cc = 0; cc < kPackChunks; ++cc) {
+      const int64_t j = (c0 + cc) * 64 + 4 * hl;  // L % 4 == 0: a group is entirely kept or not
+      const bool ok = j < L && row < M;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) k[cc][q] = ok ? __ldg(idx + j + q) : -1;
+    }
+    uint32_t ev[kPackChunks][4];
+#pragma unroll
+    for (int cc = 0; cc < kPackChunks; ++cc)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ev[cc][q] = k[cc][q] >= 0 ? static_cast<uint32_t>(__ldg(wrow + k[cc][q])) : 0u;
+#pragma unroll
+    for (int cc = 0; cc < kPackChunks; ++cc) {
+      const int64_t c = c0 + cc;
+      if (c >= nch) break;  // uniform over the warp
+      uint32_t nib = 0x4u, v01 = 0u;
+      if (k[cc][0] >= 0) {
+        nib = top2_nibble(ev[cc][0] & 0x7FFFu, ev[cc][1] & 0x7FFFu, ev[cc][2] & 0x7FFFu, ev[cc][3] & 0x7FFFu);
         const uint32_t j0 = nib & 3u, j1 = nib >> 2;
-        v01 = __byte_perm(e0 | (e1 << 16), e2 | (e3 << 16),
+        v01 = __byte_perm(ev[cc][0] | (ev[cc][1] << 16), ev[cc][2] | (ev[cc][3] << 16),
                           (2 * j0) | ((2 * j0 + 1) << 4) | ((2 * j1) << 8) | ((2 * j1 + 1) << 12));
       }
-      *reinterpret_cast<uint32_t*>(packed + 64 * P + 4096 * c + 32 * r + 2 * lane) = v01;
-    }
-    // the 16 nibbles of this row and chunk: lanes 0-7 form word 0, lanes 8-15 word 1
-    uint32_t word = (lane < 16) ? (nib << (4 * (lane & 7))) : 0u;
+      *reinterpret_cast<uint32_t*>(packed + 64 * P + 4096 * c + 32 * r + 2 * hl) = v01;
+      // the 16 nibbles of this row and chunk: lanes 0-7 of the half form word 0,
+      // lanes 8-15 word 1
+      uint32_t word = nib << (4 * (hl & 7u));
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
-    const uint32_t word1 = __shfl_sync(0xffffffffu, word, 8);
-    if (lane == 0) {
-      *reinterpret_cast<uint2*>(meta + 16 * P + r * (R / 8) + 8 * c) = make_uint2(word, word1);
-      s_words[warp][0] = word;
-      s_words[warp][1] = word1;
-    }
-    __syncthreads();
-    if (lane == 0) {
-      // tensor-core operand order: rows r and r ^ 8 share a word per 32-column span
-      uint32_t hw[2];
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const uint32_t own = s_words[warp][jj], partner = s_words[warp ^ 8][jj];
-        hw[jj] = (warp & 8) ? ((partner >> 16) | (own & 0xFFFF0000u)) : ((own & 0xFFFFu) | (partner << 16));
+      for (int o = 1; o < 8; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
+      const uint32_t w0 = __shfl_sync(0xffffffffu, word, 16 * half);
+      const uint32_t w1 = __shfl_sync(0xffffffffu, word, 16 * half + 8);
+      // tensor-core operand order: rows r and r + 8 share a word per 32-column span
+      const uint32_t p0 = __shfl_xor_sync(0xffffffffu, w0, 16), p1 = __shfl_xor_sync(0xffffffffu, w1, 16);
+      if (hl == 0) {
+        *reinterpret_cast<uint2*>(meta + 16 * P + r * (nch * 8) + 8 * c) = make_uint2(w0, w1);
+        const uint32_t h0 = half ? ((p0 >> 16) | (w0 & 0xFFFF0000u)) : ((w0 & 0xFFFFu) | (p0 << 16));
+        const uint32_t h1 = half ? ((p1 >> 16) | (w1 & 0xFFFF0000u)) : ((w1 & 0xFFFFu) | (p1 << 16));
+        *reinterpret_cast<uint4*>(meta_hw + 2048 * (Q + c) + 16 * r) = make_uint4(h0, 0u, h1, 0u);
       }
-      *reinterpret_cast<uint4*>(meta_hw + 2048 * (Q + c) + 16 * r) = make_uint4(hw[0], 0u, hw[1], 0u);
     }
   }
 }
@@ -258,23 +331,23 @@ cudaError_t launch_bw_prune(int dt, const void* W, int64_t M, int64_t K, int64_t
   const auto* w8 = static_cast<const uint8_t*>(W);
   const bool vec_ok = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && ((ldw * 2) % 16 == 0);
   cudaError_t e;
-  dim3 g(static_cast<unsigned>(ceil_div(ceil_div(K, 8), 256)), static_cast<unsigned>(tabs.nt));
+  dim3 g(static_cast<unsigned>(ceil_div(K, 128)), static_cast<unsigned>(tabs.nt));
   if (dt == SSDNN_BF16)
-    k_tw_score<1><<<g, 256, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
+    k_tw_score<1><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
   else
-    k_tw_score<0><<<g, 256, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
+    k_tw_score<0><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t nb_all = tabs.nt * (K / 64);
   k_bw_block_scores<<<static_cast<unsigned>(ceil_div(nb_all, 256)), 256, 0, s>>>(scores, K, tabs.nt, block_scores);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the tile-wise top-L selection, over blocks: (score descending, index ascending)
-  k_tw_select<<<static_cast<unsigned>(tabs.nt), 1024, 0, s>>>(block_scores, K / 64, blk_offsets, blk_indices);
+  k_tw_select<1024><<<static_cast<unsigned>(tabs.nt), 1024, 0, s>>>(block_scores, K / 64, blk_offsets, blk_indices);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (n_blocks == 0) return cudaSuccess;
   k_bw_expand<<<static_cast<unsigned>(ceil_div(64 * n_blocks, 256)), 256, 0, s>>>(blk_indices, n_blocks, col_indices);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the kept columns packed exactly as a tile-wise operand
-  dim3 gp(static_cast<unsigned>((tabs.max_R / 64) * 8), static_cast<unsigned>(tabs.nt));
+  dim3 gp(static_cast<unsigned>(ceil_div(tabs.max_R / 64, kPackChunks) * 8), static_cast<unsigned>(tabs.nt));
   auto* pk = static_cast<uint16_t*>(packed);
   if (dt == SSDNN_BF16)
     k_tw_pack<1, false><<<gp, 512, 0, s>>>(w8, M, ldw * 2, col_offsets, col_indices, schedule, pk, nullptr, nullptr);
@@ -286,7 +359,7 @@ cudaError_t launch_bw_prune(int dt, const void* W, int64_t M, int64_t K, int64_t
 cudaError_t launch_row_select(const float* scores, int64_t rows, int64_t K, const int32_t* offsets, int32_t* indices,
                               cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  k_tw_select<<<static_cast<unsigned>(rows), 1024, 0, s>>>(scores, K, offsets, indices);
+  k_tw_select<256><<<static_cast<unsigned>(rows), 256, 0, s>>>(scores, K, offsets, indices);
   return cudaGetLastError();
 }
 
@@ -300,17 +373,19 @@ cudaError_t launch_tw_prune(int dt, int tvw, const void* W, int64_t M, int64_t K
   const bool vec_ok = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && ((ldw * 2) % 16 == 0);
   cudaError_t e;
   if (K > 0) {
-    dim3 g(static_cast<unsigned>(ceil_div(ceil_div(K, 8), 256)), static_cast<unsigned>(tabs.nt));
+    dim3 g(static_cast<unsigned>(ceil_div(K, 128)), static_cast<unsigned>(tabs.nt));
     if (dt == SSDNN_BF16)
-      k_tw_score<1><<<g, 256, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
+      k_tw_score<1><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
     else
-      k_tw_score<0><<<g, 256, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
+      k_tw_score<0><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_tw_select<<<static_cast<unsigned>(tabs.nt), 1024, 0, s>>>(scores, K, offsets, indices);
+    k_tw_select<1024><<<static_cast<unsigned>(tabs.nt), 1024, 0, s>>>(scores, K, offsets, indices);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (tabs.max_R > 0) {
-    dim3 g(static_cast<unsigned>((tabs.max_R / 64) * 8), static_cast<unsigned>(tabs.nt));
+    // 16 rows (TW) or 32 rows (TVW) and kPackChunks chunks per CTA
+    const unsigned cg = static_cast<unsigned>(ceil_div(tabs.max_R / 64, kPackChunks));
+    dim3 g(cg * (tvw ? 4u : 8u), static_cast<unsigned>(tabs.nt));
     auto* pk = static_cast<uint16_t*>(packed);
     if (dt == SSDNN_BF16) {
       if (tvw)

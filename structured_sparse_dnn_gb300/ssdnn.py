@@ -284,11 +284,24 @@ def tw_sizes(dt: int, tvw: bool, M: int, K: int, keep) -> dict:
                     (o.value for o in out)))
 
 
-def tw_prune_compress(W: torch.Tensor, keep, tvw: bool, workspace: torch.Tensor | None = None) -> TileWise:
+def tw_prune_compress(W: torch.Tensor, keep, tvw: bool, workspace: torch.Tensor | None = None,
+                      out: TileWise | None = None) -> TileWise:
+    """Tile-wise (tvw=False) or tile-vector-wise prune + pack. `out`, a result of an
+    earlier call with the same shape, type, pattern and kept counts, is overwritten
+    in place (no allocation)."""
     dt = _DT[W.dtype]
     M, K = W.shape
     assert W.stride(1) == 1
     k = _keep_arr(keep)
+    if out is not None:
+        if (out.dt, out.tvw, out.M, out.K) != (dt, bool(tvw), M, K) or not np.array_equal(out.keep, k):
+            raise ValueError("tw_prune_compress: out was made for another weight shape or kept counts")
+        if workspace is None:
+            raise ValueError("tw_prune_compress: out= needs a workspace")
+        _check(lib.tw_prune_compress(dt, int(tvw), _p(W), M, K, W.stride(0), _kp(out.keep), _p(out.offsets),
+                                     _p(out.indices), _p(out.schedule), _p(out.packed), _p(out.meta),
+                                     _p(out.meta_hw), _p(workspace), _stream(W.device)), "tw_prune_compress")
+        return out
     sz = tw_sizes(dt, tvw, M, K, k)
     dev = W.device
     nt = (M + 127) // 128
@@ -375,11 +388,23 @@ def bw_sizes(dt: int, M: int, K: int, keep_blocks) -> dict:
     return dict(zip(("packed_bytes", "indices_count", "workspace_bytes"), (o.value for o in out)))
 
 
-def bw_prune_compress(W: torch.Tensor, keep_blocks, workspace: torch.Tensor | None = None) -> BlockWise:
+def bw_prune_compress(W: torch.Tensor, keep_blocks, workspace: torch.Tensor | None = None,
+                      out: BlockWise | None = None) -> BlockWise:
+    """Block-wise prune + pack. `out`, a result of an earlier call with the same
+    shape, type and kept block counts, is overwritten in place (no allocation)."""
     dt = _DT[W.dtype]
     M, K = W.shape
     assert W.stride(1) == 1
     k = _keep_arr(keep_blocks)
+    if out is not None:
+        if (out.dt, out.M, out.K) != (dt, M, K) or not np.array_equal(out.keep, k):
+            raise ValueError("bw_prune_compress: out was made for another weight shape or kept counts")
+        if workspace is None:
+            raise ValueError("bw_prune_compress: out= needs a workspace")
+        _check(lib.bw_prune_compress(dt, _p(W), M, K, W.stride(0), _kp(out.keep), _p(out.offsets), _p(out.indices),
+                                     _p(out.schedule), _p(out.packed), _p(workspace), _stream(W.device)),
+               "bw_prune_compress")
+        return out
     sz = bw_sizes(dt, M, K, k)
     dev = W.device
     nt = (M + 127) // 128
@@ -434,10 +459,21 @@ def ew_sizes(dt: int, M: int, K: int, k: int) -> dict:
     return dict(zip(("vals_bytes", "indices_count", "workspace_bytes"), (o.value for o in out)))
 
 
-def ew_prune_compress(W: torch.Tensor, k: int, workspace: torch.Tensor | None = None) -> ElementWise:
+def ew_prune_compress(W: torch.Tensor, k: int, workspace: torch.Tensor | None = None,
+                      out: ElementWise | None = None) -> ElementWise:
+    """Element-wise prune to CSR (k kept per row). `out`, a result of an earlier call
+    with the same shape, type and k, is overwritten in place (no allocation)."""
     dt = _DT[W.dtype]
     M, K = W.shape
     assert W.stride(1) == 1
+    if out is not None:
+        if (out.dt, out.M, out.K, out.k) != (dt, M, K, k):
+            raise ValueError("ew_prune_compress: out was made for another weight shape or k")
+        if workspace is None:
+            raise ValueError("ew_prune_compress: out= needs a workspace")
+        _check(lib.ew_prune_compress(dt, _p(W), M, K, W.stride(0), k, _p(out.row_ptr), _p(out.col_buf),
+                                     _p(out.val_buf), _p(workspace), _stream(W.device)), "ew_prune_compress")
+        return out
     sz = ew_sizes(dt, M, K, k)
     dev = W.device
     row_ptr = torch.empty(M + 1, dtype=torch.int32, device=dev)

@@ -77,3 +77,50 @@ def test_full_keep_matches_dense_gemm_bits_within_bound():
     Y_ref = oracle.gemm.gemm_dense(W, X, "bf16", "bf16")
     B = oracle.gemm.bound(W, X, "bf16")
     assert oracle.gemm.within_bound(bits_of(Y), Y_ref, B, "bf16", 1e-2).all()
+
+
+@pytest.mark.parametrize("pattern", ["tw", "tvw", "bw", "ew"])
+def test_prune_into_existing_result_matches_fresh(pattern):
+    """out= overwrites an earlier result in place: pruning a second weight into the
+    first weight's buffers gives exactly what a fresh call on it gives."""
+    ss = lib()
+    M, K, dt = 384, 512, "bf16"
+    W1 = dev_tensor(rand_bits(901, (M, K), dt, 0.02), dt)
+    W2 = dev_tensor(rand_bits(902, (M, K), dt, 0.02), dt)
+    if pattern in ("tw", "tvw"):
+        keep = np.array([128, 64, 256], dtype=np.int32)
+        tvw = pattern == "tvw"
+        work = torch.empty(ss.tw_sizes(ss.BF16, tvw, M, K, keep)["workspace_bytes"], dtype=torch.uint8,
+                           device="cuda")
+        form = ss.tw_prune_compress(W1, keep, tvw, work)
+        fresh = ss.tw_prune_compress(W2, keep, tvw, work)
+        again = ss.tw_prune_compress(W2, keep, tvw, work, out=form)
+        names = ["offsets", "indices", "schedule", "packed"] + (["meta", "meta_hw"] if tvw else [])
+    elif pattern == "bw":
+        keep = np.array([2, 0, 8], dtype=np.int32)
+        work = torch.empty(ss.bw_sizes(ss.BF16, M, K, keep)["workspace_bytes"], dtype=torch.uint8, device="cuda")
+        form = ss.bw_prune_compress(W1, keep, work)
+        fresh = ss.bw_prune_compress(W2, keep, work)
+        again = ss.bw_prune_compress(W2, keep, work, out=form)
+        names = ["offsets", "indices", "schedule", "packed"]
+    else:
+        k = 51
+        work = torch.empty(ss.ew_sizes(ss.BF16, M, K, k)["workspace_bytes"], dtype=torch.uint8, device="cuda")
+        form = ss.ew_prune_compress(W1, k, work)
+        fresh = ss.ew_prune_compress(W2, k, work)
+        again = ss.ew_prune_compress(W2, k, work, out=form)
+        names = ["row_ptr", "col_idx", "vals"]
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
+    assert again is form
+    for n in names:
+        a, b = getattr(again, n), getattr(fresh, n)
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
+                           b.view(torch.uint8) if b.dtype != torch.int32 else b), n
+    with pytest.raises(ValueError):
+        if pattern in ("tw", "tvw"):
+            ss.tw_prune_compress(W2, keep + 4, pattern == "tvw", work, out=form)
+        elif pattern == "bw":
+            ss.bw_prune_compress(W2, keep + 1, work, out=form)
+        else:
+            ss.ew_prune_compress(W2, k + 1, work, out=form)
