@@ -5,8 +5,8 @@
 One JSON line on rank 0. A step is one sparse GEMM Y = W_sparse . X over the
 workload's activation batch, with the 2:4-compressed weight resident in HBM
 (weights are pruned and compressed once; the per-step work is the GEMM). L2 is
-flushed (a 256 MB write) between timed steps; each step is timed with CUDA
-events on the launching stream. The other hot-path rows (prune/compress, the
+flushed (a write of twice the device's L2, at least 256 MB) between timed steps;
+each step is timed with CUDA events on the launching stream. The other hot-path rows (prune/compress, the
 tile-wise prune, the TW/TVW gather GEMMs and the dense GEMM of the same kernel
 family) are timed the same way and reported under "rows".
 
@@ -36,7 +36,14 @@ from structured_sparse_dnn_gb300 import inputs as I  # noqa: E402
 METRIC = "effective TFLOP/s and % of 2:4-sparse tensor peak for sparse GEMM (1×GB300)"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "llm_ffn_e4m3"
-FLUSH_BYTES = 256 << 20
+FLUSH_BYTES = 256 << 20   # the least L2 flush; flush_bytes() takes twice the device's L2 if larger
+
+
+def flush_bytes(dev) -> int:
+    """Size of the buffer written between timed steps: twice the device's L2 (read from
+    the device, not assumed), at least FLUSH_BYTES, rounded to 1 MB."""
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 0)
+    return max(FLUSH_BYTES, (2 * l2 + (1 << 20) - 1) >> 20 << 20)
 
 
 def peaks() -> dict:
@@ -222,7 +229,8 @@ def headline_protocol(step, flush, stream, dev, eff_flops) -> dict:
                                  "median_TFLOP/s": tf(statistics.median(eager))},
             "graph_l2_warm": {"launches": n, "ms_per_launch": round(warm, 5), "TFLOP/s": tf(warm)},
             "graph_l2_flushed": {"launches": n, "ms_per_launch": round(cold, 5), "TFLOP/s": tf(cold),
-                                 "note": "50 (256 MB flush, GEMM) pairs in one graph minus 50 flushes alone"}}
+                                 "note": f"50 (flush of {flush.numel() * 4 >> 20} MB, GEMM) pairs in one graph minus "
+                                         "50 flushes alone"}}
 
 
 def host_link_rates(X_dev, X_host, Y_dev, Y_host, stream) -> dict:
@@ -311,7 +319,8 @@ def run_gpu(args) -> None:
     pk = peaks()
     wl = I.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    fbytes = flush_bytes(dev)
+    flush = torch.empty(fbytes // 4, dtype=torch.float32, device=dev)
     d, Wd, Xd, form = make_sp24(wl, dev, ss)
     M, K, N = wl.M, wl.K, wl.N
     Y = torch.empty((M, N), dtype=torch.bfloat16 if wl.out_dt == "bf16" else torch.float16, device=dev)
@@ -396,7 +405,7 @@ def run_gpu(args) -> None:
             "config": {"workload": f"{wl.name}: W {M}x{K} N(0,{wl.sigma_w:g}) pruned 2:4, X {K}x{N} N(0,1), "
                                    f"{wl.dt} in, {wl.out_dt} out, fp32 accumulate",
                        "M": M, "K": K, "N": N, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": "flushed between timed steps (256 MB write)"},
+                       "l2": f"flushed between timed steps ({fbytes >> 20} MB write, >= 2x the device's L2)"},
             "step_ms": {"min": round(min(times), 5), "p10": round(pct(times, 10), 5),
                         "median": round(statistics.median(times), 5), "p90": round(pct(times, 90), 5),
                         "max": round(max(times), 5)},
