@@ -331,8 +331,9 @@ def run_gpu(args) -> None:
         ss.sp24_gemm(form, Xd, alpha=alpha, out=Y)
 
     # ---- timed region: K steps, barrier + synchronize on both sides, clocks sampled
-    # (the sampler also covers about half a second of untimed warm-up GEMMs so that
-    # it sees the GPU under load)
+    # (the sampler also covers about half a second of untimed warm-up steps so that
+    # it sees the GPU under load; they repeat the timed pattern, an L2 flush then the
+    # GEMM, so that the power and clock state they leave is the timed steps' own)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -343,6 +344,7 @@ def run_gpu(args) -> None:
         t0 = time.perf_counter()
         while time.perf_counter() - t0 < 0.5:
             for _ in range(20):
+                flush.fill_(1)
                 step()
             torch.cuda.synchronize()
         times = timed_steps(step, args.steps, 0, flush, stream)

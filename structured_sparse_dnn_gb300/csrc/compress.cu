@@ -6,14 +6,17 @@
 // Criterion (reading): keep the two largest |w| of each group, ties to the lower
 // position, comparing the stored bits with the sign cleared as integers.
 //
-// One thread owns 32 consecutive elements of a row (8 groups): 64 B of fp16/bf16
-// or 32 B of e4m3 read with 16-byte loads, 32 B / 16 B of values and 4 B of
-// canonical metadata written, plus the word of the tensor-core operand layout of
-// the metadata. The grid also covers the 128-row and K-block padding of that
+// A thread owns 32 consecutive elements of a row (8 groups; e4m3: two adjacent such
+// chunks): 64 B of fp16/bf16 or 2 x 32 B of e4m3 read with 16-byte loads, 32 B /
+// 2 x 16 B of values and 4 B of canonical metadata per chunk written, plus its part
+// of the tensor-core operand layout of the metadata. The grid also covers the 128-row and K-block padding of that
 // layout, which it fills with the (0,1) pattern. A group's kept pair comes from six
-// pairwise magnitude comparisons made in parallel on the group's packed bytes
-// (e4m3) or 16-bit lanes, looked up in a 64-entry table of kept pairs (e4m3: a byte
-// table of selectors, four groups' selectors combined in one word).
+// pairwise magnitude comparisons, looked up in a 64-entry table of kept pairs. For
+// e4m3 the comparisons of four groups are made together: their four words are
+// transposed (word p = position p of each group) and each comparison is one
+// byte-parallel subtraction; the table is of byte selectors, and four groups'
+// selectors are combined in one word. For fp16/bf16 the comparisons are made on the
+// 16-bit lanes of one group's two words.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -46,19 +49,30 @@ __device__ __forceinline__ uint32_t kept_pair_entry(uint32_t idx, int eb) {
   return nib | (((2 * j0) | ((2 * j0 + 1) << 4) | ((2 * j1) << 8) | ((2 * j1 + 1) << 12)) << 8);
 }
 
-// The six order bits of a group of four e4m3 codes in one word (byte i = code i):
-// byte-parallel subtractions with a guard bit (magnitudes are 7 bits).
-__device__ __forceinline__ uint32_t order_bits_e4m3(uint32_t w) {
-  const uint32_t m = w & 0x7F7F7F7Fu;
-  const uint32_t mo = m | 0x80808080u;
-  const uint32_t r1 = __byte_perm(m, 0u, 0x0321);  // byte i: m_{(i+1) % 4}
-  const uint32_t r2 = __byte_perm(m, 0u, 0x1032);  // byte i: m_{(i+2) % 4}
-  // bit 7 of byte i: [m_i >= m_{i+1}] (byte 3 strict: [m_3 > m_0]); bits 7, 15: [m0 >= m2], [m1 >= m3]
-  const uint32_t ge1 = (mo - r1 - 0x01000000u) & 0x80808080u;
-  const uint32_t ge2 = (mo - r2) & 0x00008080u;
-  // gather bits 7, 15, 23, 31 of ge1 and 7, 15 of ge2 into bits 24..29
-  const uint32_t z = (ge1 >> 7) | (ge2 >> 3);
-  return (z * 0x01020408u) >> 24;
+// The order indices of four groups of four e4m3 codes (one group per word, byte i =
+// code i), one per byte of the result: byte g = r_g = b5 | b4 << 1 | b3 << 2 | b2 << 3 |
+// b1 << 4 | b0 << 5, group g's order bits in reversed order. The words are
+// transposed so that t_p holds the code at position p of all four groups; each
+// comparison is then one byte-parallel subtraction with a guard bit (magnitudes are
+// 7 bits, so 0x80 + m_a - m_b never borrows across bytes and its bit 7 is
+// [m_a >= m_b]; with 0x7F it is [m_a > m_b]).
+__device__ __forceinline__ uint32_t order_index4_e4m3(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  const uint32_t x01l = __byte_perm(w0, w1, 0x5140), x01h = __byte_perm(w0, w1, 0x7362);
+  const uint32_t x23l = __byte_perm(w2, w3, 0x5140), x23h = __byte_perm(w2, w3, 0x7362);
+  const uint32_t t0 = __byte_perm(x01l, x23l, 0x5410) & 0x7F7F7F7Fu;
+  const uint32_t t1 = __byte_perm(x01l, x23l, 0x7632) & 0x7F7F7F7Fu;
+  const uint32_t t2 = __byte_perm(x01h, x23h, 0x5410) & 0x7F7F7F7Fu;
+  const uint32_t t3 = __byte_perm(x01h, x23h, 0x7632) & 0x7F7F7F7Fu;
+  const uint32_t e01 = t0 - t1 + 0x80808080u, e12 = t1 - t2 + 0x80808080u, e23 = t2 - t3 + 0x80808080u;
+  const uint32_t e30 = t3 - t0 + 0x7F7F7F7Fu, e02 = t0 - t2 + 0x80808080u, e13 = t1 - t3 + 0x80808080u;
+  // bit 7 of each byte of e01, e12, e23, e30, e02, e13 to bits 5..0
+  uint32_t v = (e01 >> 2) & 0x20202020u;
+  v = (v & 0x20202020u) | ((e12 >> 3) & 0x1F1F1F1Fu);
+  v = (v & 0x30303030u) | ((e23 >> 4) & 0x0F0F0F0Fu);
+  v = (v & 0x38383838u) | ((e30 >> 5) & 0x07070707u);
+  v = (v & 0x3C3C3C3Cu) | ((e02 >> 6) & 0x03030303u);
+  v = (v & 0x3E3E3E3Eu) | ((e13 >> 7) & 0x01010101u);
+  return v;
 }
 
 // The same for a group of four 16-bit codes in two words (lo = v0 | v1 << 16,
@@ -81,24 +95,128 @@ __device__ __forceinline__ uint32_t order_bits_16(uint32_t lo, uint32_t hi) {
   return (z * 0x01020408u) >> 24;
 }
 
-// A thread owns CPT chunks of 32 consecutive elements of a row (8 groups each):
-// 64 B (fp16/bf16, one chunk) or 2 x 32 B (e4m3, two adjacent chunks), all loaded
-// before any is processed; block = 16 rows x 16 threads; grid.y walks 16-row
-// groups of the 128-row-padded matrix.
+// Shared-memory tables of a block: the kept-pair entries (fp16/bf16), the e4m3 byte
+// selectors at the bit-reversed order index, and the rows' metadata words exchanged
+// for the 16-bit operand order.
+struct CompressShared {
+  uint32_t tab[64];
+  uint8_t sel[64];
+  uint32_t nib[16][17];
+};
+
+// Threads 0..63 fill the tables (the caller synchronises before use).
+__device__ __forceinline__ void build_tables(CompressShared& sh, int eb) {
+  if (threadIdx.x < 64) {
+    const uint32_t e = kept_pair_entry(threadIdx.x, eb);
+    sh.tab[threadIdx.x] = e;
+    // e4m3: the same entry at the bit-reversed index (the four-group order index)
+    sh.sel[__brev(threadIdx.x) >> 26] = static_cast<uint8_t>(e >> 8);
+  }
+}
+
+// The work of one thread on the codes it holds: w[cc] = chunk c0 + cc of row i (32
+// elements, zero past K and M, so that such groups take the (0, 1) entry: nibble 0x4
+// and zero values). Writes the kept values, the canonical nibbles (if meta) and the
+// operand-order metadata. A thread is (tr, tc) of a 16 x 16 block that covers 16
+// consecutive rows; every thread of the block calls it (16-bit: one barrier inside).
 template <int EB>
-__global__ void __launch_bounds__(256) k_sp24_compress(const uint8_t* __restrict__ W, int64_t M, int64_t K,
+__device__ __forceinline__ void compress_store(const uint32_t (&w)[EB == 1 ? 2 : 1][16], int64_t i, int64_t c0,
+                                               int tr, int tc, int64_t M, int64_t Kp, uint8_t* __restrict__ values,
+                                               int64_t ldv_b, uint8_t* __restrict__ meta, int64_t ldm,
+                                               uint8_t* __restrict__ meta_hw, int64_t KBhw, int64_t chunks_pad,
+                                               CompressShared& sh) {
+  constexpr int CPT = EB == 1 ? 2 : 1;
+  uint32_t nib[CPT];
+  uint32_t outv[CPT][8];  // 16 kept values (EB bytes each) per chunk
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) {
+    uint32_t nw = 0;
+    if constexpr (EB == 1) {
+      // the groups' selector bytes j0 | j1 << 4, four to a word
+      uint32_t sb[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t v = order_index4_e4m3(w[cc][4 * h], w[cc][4 * h + 1], w[cc][4 * h + 2], w[cc][4 * h + 3]);
+        sb[4 * h] = sh.sel[v & 0xFFu];
+        sb[4 * h + 1] = sh.sel[__byte_perm(v, 0u, 0x4441)];
+        sb[4 * h + 2] = sh.sel[__byte_perm(v, 0u, 0x4442)];
+        sb[4 * h + 3] = sh.sel[v >> 24];
+      }
+      const uint32_t S0 = __byte_perm(__byte_perm(sb[0], sb[1], 0x0040), __byte_perm(sb[2], sb[3], 0x0040), 0x5410);
+      const uint32_t S1 = __byte_perm(__byte_perm(sb[4], sb[5], 0x0040), __byte_perm(sb[6], sb[7], 0x0040), 0x5410);
+      // output word of groups (g, g + 1): selector j0 | j1 << 4 | (j0' + 4) << 8 | (j1' + 4) << 12
+      outv[cc][0] = __byte_perm(w[cc][0], w[cc][1], S0 + 0x4400u);
+      outv[cc][1] = __byte_perm(w[cc][2], w[cc][3], (S0 >> 16) + 0x4400u);
+      outv[cc][2] = __byte_perm(w[cc][4], w[cc][5], S1 + 0x4400u);
+      outv[cc][3] = __byte_perm(w[cc][6], w[cc][7], (S1 >> 16) + 0x4400u);
+#pragma unroll
+      for (int q = 4; q < 8; ++q) outv[cc][q] = 0u;
+      // nibble j0 | j1 << 2 of each selector byte, then the bytes' nibbles packed in order
+      auto nibbles = [](uint32_t S) {
+        const uint32_t n = (S | (S >> 2)) & 0x0F0F0F0Fu;
+        const uint32_t t = (n | (n >> 4)) & 0x00FF00FFu;
+        return (t | (t >> 8)) & 0xFFFFu;
+      };
+      nw = nibbles(S0) | (nibbles(S1) << 16);
+    } else {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t e = sh.tab[order_bits_16(w[cc][2 * g], w[cc][2 * g + 1])];
+        nw |= (e & 0xFu) << (4 * g);
+        outv[cc][g] = __byte_perm(w[cc][2 * g], w[cc][2 * g + 1], e >> 8);
+      }
+    }
+    nib[cc] = nw;
+  }
+  if (i < M) {
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) {
+      const int64_t c = c0 + cc;
+      if (c * 32 >= Kp) break;
+      uint8_t* dv = values + i * ldv_b + c * 16 * EB;
+      reinterpret_cast<uint4*>(dv)[0] = make_uint4(outv[cc][0], outv[cc][1], outv[cc][2], outv[cc][3]);
+      if constexpr (EB == 2)
+        reinterpret_cast<uint4*>(dv)[1] = make_uint4(outv[cc][4], outv[cc][5], outv[cc][6], outv[cc][7]);
+      if (meta) *reinterpret_cast<uint32_t*>(meta + i * ldm + c * 4) = nib[cc];
+    }
+  }
+  const int64_t mb = i >> 7, r = i & 127;
+  if constexpr (EB == 1) {
+    // e4m3 operand order = canonical nibbles, 16 bytes per row per 128 columns of K
+    // (the thread's two chunks are adjacent: 8 bytes, one store)
+    if (c0 < chunks_pad)
+      *reinterpret_cast<uint2*>(meta_hw + ((mb * KBhw + (c0 >> 2)) * 128 + r) * 16 + (c0 & 3) * 4) =
+          make_uint2(nib[0], nib[1]);
+  } else {
+    // 16-bit operand order: rows r and r ^ 8 share one 32-bit word per 32-column
+    // span (lower row: groups 0..3 of both rows; upper row: groups 4..7 of both),
+    // each span in its own even TMEM column (odd words zero).
+    sh.nib[tr][tc] = nib[0];
+    __syncthreads();
+    const uint32_t partner = sh.nib[tr ^ 8][tc];
+    const uint32_t hw =
+        (tr & 8) ? ((partner >> 16) | (nib[0] & 0xFFFF0000u)) : ((nib[0] & 0xFFFFu) | (partner << 16));
+    if (c0 < chunks_pad)
+      *reinterpret_cast<uint2*>(meta_hw + ((mb * KBhw + (c0 >> 1)) * 128 + r) * 16 + (c0 & 1) * 8) =
+          make_uint2(hw, 0u);
+  }
+}
+
+// A thread owns CPT chunks of 32 consecutive elements of a row (8 groups each): 64 B
+// (fp16/bf16, one chunk) or 2 x 32 B (e4m3, two adjacent chunks), all loaded before
+// any is processed; block = 16 rows x 16 threads, eight blocks per SM (at most 32
+// registers a thread); grid.y walks 16-row groups of the 128-row-padded matrix.
+template <int EB>
+__global__ void __launch_bounds__(256, 8) k_sp24_compress(const uint8_t* __restrict__ W, int64_t M, int64_t K,
                                                        int64_t ldw_b, uint8_t* __restrict__ values,
                                                        int64_t ldv_b, uint8_t* __restrict__ meta, int64_t ldm,
                                                        uint8_t* __restrict__ meta_hw, int64_t KBhw,
                                                        int64_t chunks_pad, bool vec_ok) {
   constexpr int CPT = EB == 1 ? 2 : 1;  // chunks per thread
-  __shared__ uint32_t s_nib[16][17];
-  __shared__ uint32_t s_tab[64];
-  __shared__ uint8_t s_sel[64];  // e4m3: j0 | j1 << 4 of the kept pair (one byte: no bank conflicts)
+  __shared__ CompressShared sh;
   const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
   const int64_t i = static_cast<int64_t>(blockIdx.y) * 16 + tr;
   const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 16 + tc) * CPT;  // first chunk
-  const int64_t Kp = (K + 31) / 32 * 32;
 
   uint32_t w[CPT][16];
 #pragma unroll
@@ -130,115 +248,35 @@ __global__ void __launch_bounds__(256) k_sp24_compress(const uint8_t* __restrict
       }
     }
   }
-
-  // the kept-pair table, built while the loads are in flight
-  if (threadIdx.x < 64) {
-    const uint32_t e = kept_pair_entry(threadIdx.x, EB);
-    s_tab[threadIdx.x] = e;
-    s_sel[threadIdx.x] = static_cast<uint8_t>(e >> 8);
-  }
+  build_tables(sh, EB);  // while the loads are in flight
   __syncthreads();
-
-  uint32_t nib[CPT];
-  uint32_t outv[CPT][8];  // 16 kept values (EB bytes each) per chunk
-#pragma unroll
-  for (int cc = 0; cc < CPT; ++cc) {
-    const int64_t k0 = (c0 + cc) * 32;
-    // groups past K (K % 4 == 0: a group is entirely in or out) take the (0, 1)
-    // entry: nibble 0x4, the zero values loaded there
-    const int ngroups = (i >= M || k0 >= K) ? 0 : ((K - k0) / 4 < 8 ? static_cast<int>((K - k0) / 4) : 8);
-    uint32_t nw = 0;
-    if constexpr (EB == 1) {
-      // the groups' selector bytes j0 | j1 << 4 (groups past K: (0, 1)), four to a word
-      uint32_t sb[8];
-      if (ngroups == 8) {
-#pragma unroll
-        for (int g = 0; g < 8; ++g) sb[g] = s_sel[order_bits_e4m3(w[cc][g])];
-      } else {
-#pragma unroll
-        for (int g = 0; g < 8; ++g) sb[g] = g < ngroups ? s_sel[order_bits_e4m3(w[cc][g])] : 0x10u;
-      }
-      const uint32_t S0 = __byte_perm(__byte_perm(sb[0], sb[1], 0x0040), __byte_perm(sb[2], sb[3], 0x0040), 0x5410);
-      const uint32_t S1 = __byte_perm(__byte_perm(sb[4], sb[5], 0x0040), __byte_perm(sb[6], sb[7], 0x0040), 0x5410);
-      // output word of groups (g, g + 1): selector j0 | j1 << 4 | (j0' + 4) << 8 | (j1' + 4) << 12
-      outv[cc][0] = __byte_perm(w[cc][0], w[cc][1], S0 + 0x4400u);
-      outv[cc][1] = __byte_perm(w[cc][2], w[cc][3], (S0 >> 16) + 0x4400u);
-      outv[cc][2] = __byte_perm(w[cc][4], w[cc][5], S1 + 0x4400u);
-      outv[cc][3] = __byte_perm(w[cc][6], w[cc][7], (S1 >> 16) + 0x4400u);
-#pragma unroll
-      for (int q = 4; q < 8; ++q) outv[cc][q] = 0u;
-      // nibble j0 | j1 << 2 of each selector byte, then the bytes' nibbles packed in order
-      auto nibbles = [](uint32_t S) {
-        const uint32_t n = (S | (S >> 2)) & 0x0F0F0F0Fu;
-        const uint32_t t = (n | (n >> 4)) & 0x00FF00FFu;
-        return (t | (t >> 8)) & 0xFFFFu;
-      };
-      nw = nibbles(S0) | (nibbles(S1) << 16);
-    } else {
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const uint32_t e = g < ngroups ? s_tab[order_bits_16(w[cc][2 * g], w[cc][2 * g + 1])] : 0x321004u;
-        nw |= (e & 0xFu) << (4 * g);
-        outv[cc][g] = __byte_perm(w[cc][2 * g], w[cc][2 * g + 1], e >> 8);
-      }
-    }
-    nib[cc] = nw;
-  }
-  if (i < M) {
-#pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) {
-      const int64_t c = c0 + cc;
-      if (c * 32 >= Kp) break;
-      uint8_t* dv = values + i * ldv_b + c * 16 * EB;
-      reinterpret_cast<uint4*>(dv)[0] = make_uint4(outv[cc][0], outv[cc][1], outv[cc][2], outv[cc][3]);
-      if constexpr (EB == 2)
-        reinterpret_cast<uint4*>(dv)[1] = make_uint4(outv[cc][4], outv[cc][5], outv[cc][6], outv[cc][7]);
-      if (meta) *reinterpret_cast<uint32_t*>(meta + i * ldm + c * 4) = nib[cc];
-    }
-  }
-  const int64_t mb = i >> 7, r = i & 127;
-  if constexpr (EB == 1) {
-    // e4m3 operand order = canonical nibbles, 16 bytes per row per 128 columns of K
-    // (the thread's two chunks are adjacent: 8 bytes, one store)
-    if (c0 < chunks_pad)
-      *reinterpret_cast<uint2*>(meta_hw + ((mb * KBhw + (c0 >> 2)) * 128 + r) * 16 + (c0 & 3) * 4) =
-          make_uint2(nib[0], nib[1]);
-  } else {
-    // 16-bit operand order: rows r and r ^ 8 share one 32-bit word per 32-column
-    // span (lower row: groups 0..3 of both rows; upper row: groups 4..7 of both),
-    // each span in its own even TMEM column (odd words zero).
-    s_nib[tr][tc] = nib[0];
-    __syncthreads();
-    const uint32_t partner = s_nib[tr ^ 8][tc];
-    const uint32_t hw =
-        (tr & 8) ? ((partner >> 16) | (nib[0] & 0xFFFF0000u)) : ((nib[0] & 0xFFFFu) | (partner << 16));
-    if (c0 < chunks_pad)
-      *reinterpret_cast<uint2*>(meta_hw + ((mb * KBhw + (c0 >> 1)) * 128 + r) * 16 + (c0 & 1) * 8) =
-          make_uint2(hw, 0u);
-  }
+  compress_store<EB>(w, i, c0, tr, tc, M, (K + 31) / 32 * 32, values, ldv_b, meta, ldm, meta_hw, KBhw, chunks_pad,
+                     sh);
 }
 
 }  // namespace
 
 cudaError_t launch_sp24_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, void* values,
                                  uint8_t* meta, uint8_t* meta_hw, cudaStream_t s, uint32_t* err) {
-  (void)err;
+  (void)err;  // no waits in this kernel
   const int EB = (dt == SSDNN_E4M3) ? 1 : 2;
   const int64_t span = (EB == 1) ? 128 : 64;          // K columns per operand metadata block
   const int64_t MB = ceil_div(M, 128), KBhw = ceil_div(K, span);
   const int64_t chunks_pad = KBhw * (span / 32);
   if (MB == 0 || KBhw == 0) return cudaSuccess;
   const int64_t Kp = round_up(K, 32);
+  const int64_t ldv_b = Kp / 2 * EB;
   const bool vec_ok = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && ((ldw * EB) % 16 == 0);
   const int64_t cpt = EB == 1 ? 2 : 1;  // chunks per thread (chunks_pad is a multiple of 4 for e4m3)
-  const dim3 grid(static_cast<unsigned>(ceil_div(chunks_pad, 16 * cpt)), static_cast<unsigned>(MB * 8));
+  const int64_t tiles_x = ceil_div(chunks_pad, 16 * cpt), tiles_y = MB * 8;
+  const dim3 grid(static_cast<unsigned>(tiles_x), static_cast<unsigned>(tiles_y));
   if (EB == 2)
     k_sp24_compress<2><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(W), M, K, ldw * 2,
-                                            static_cast<uint8_t*>(values), Kp / 2 * 2, meta, Kp / 8, meta_hw, KBhw,
+                                            static_cast<uint8_t*>(values), ldv_b, meta, Kp / 8, meta_hw, KBhw,
                                             chunks_pad, vec_ok);
   else
     k_sp24_compress<1><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(W), M, K, ldw,
-                                            static_cast<uint8_t*>(values), Kp / 2, meta, Kp / 8, meta_hw, KBhw,
+                                            static_cast<uint8_t*>(values), ldv_b, meta, Kp / 8, meta_hw, KBhw,
                                             chunks_pad, vec_ok);
   return cudaGetLastError();
 }
