@@ -280,6 +280,35 @@ __device__ __forceinline__ float gelu_exact(float x) {
   return 0.5f * x * (x >= 0.f ? 2.f - q : q);
 }
 
+// The same GELU epilogue on two accumulator values at once (alpha times the value
+// plus the bias, GELU, the output scale), with the fp32 arithmetic on packed pairs:
+// half the instructions of two scalar calls, the same results (0.5 x r y_scale is
+// taken as (x r)(0.5 y_scale), equal to (0.5 x) r y_scale since halving is exact).
+__device__ __forceinline__ void gelu_epilogue_pair(float a0, float a1, float alpha, float b, bool has_bias,
+                                                   float y_scale, float& o0, float& o1) {
+  constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
+                  kA4 = -1.453152027f, kA5 = 1.061405429f;
+  using namespace ptx;
+  const uint64_t acc = f2_pack(a0, a1), al = f2_pack(alpha, alpha);
+  const uint64_t x = has_bias ? f2_fma(acc, al, f2_pack(b, b)) : f2_mul(acc, al);
+  const uint64_t z = f2_mul(x & 0x7FFFFFFF7FFFFFFFull, f2_pack(0.70710678118654752f, 0.70710678118654752f));
+  const uint64_t d = f2_fma(f2_pack(kP, kP), z, f2_pack(1.f, 1.f));
+  const uint64_t t = f2_pack(__fdividef(1.f, f2_lo(d)), __fdividef(1.f, f2_hi(d)));
+  uint64_t poly = f2_fma(f2_pack(kA5, kA5), t, f2_pack(kA4, kA4));
+  poly = f2_fma(poly, t, f2_pack(kA3, kA3));
+  poly = f2_fma(poly, t, f2_pack(kA2, kA2));
+  poly = f2_fma(poly, t, f2_pack(kA1, kA1));
+  poly = f2_mul(poly, t);
+  const uint64_t zz = f2_mul(z, z);
+  const uint64_t q = f2_mul(poly, f2_pack(__expf(-f2_lo(zz)), __expf(-f2_hi(zz))));
+  const float q0 = f2_lo(q), q1 = f2_hi(q);
+  const uint64_t r = f2_pack(f2_lo(x) >= 0.f ? 2.f - q0 : q0, f2_hi(x) >= 0.f ? 2.f - q1 : q1);
+  const float hs = 0.5f * y_scale;
+  const uint64_t o = f2_mul(f2_mul(x, r), f2_pack(hs, hs));
+  o0 = f2_lo(o);
+  o1 = f2_hi(o);
+}
+
 // The fused layer epilogue on one fp32 accumulator value, in this order: alpha
 // times the accumulator plus the row's bias (one fma), the activation, the
 // output scale.
@@ -766,7 +795,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]) * p.alpha;
         } else if (p.act == 2) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, 2, p.y_scale);
+          for (int i = 0; i < 32; i += 2)
+            gelu_epilogue_pair(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), p.alpha, bias, has_bias, p.y_scale,
+                               x[i], x[i + 1]);
         } else if (p.act == 1) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[i] = epilogue_value(__uint_as_float(r[i]), p.alpha, bias, has_bias, 1, p.y_scale);
