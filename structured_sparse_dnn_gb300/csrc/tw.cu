@@ -119,7 +119,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* ws, ui
 // NT threads per CTA: 1024 for the few tiles of a tile-wise weight (the CTA's latency
 // is the kernel's), 256 for the many rows of the element-wise prune (more CTAs per SM).
 template <int NT>
-__global__ void __launch_bounds__(NT) k_tw_select(const float* __restrict__ scores, int64_t K,
+__global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : 4) k_tw_select(const float* __restrict__ scores, int64_t K,
                                                     const int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ indices) {
   __shared__ uint32_t hist[256];
@@ -131,14 +131,36 @@ __global__ void __launch_bounds__(NT) k_tw_select(const float* __restrict__ scor
   int32_t* out = indices + offsets[t];
   const uint32_t* key = reinterpret_cast<const uint32_t*>(scores + t * K);
 
+  // up to 4096 keys stay in registers (KPT a thread) for the four passes and the
+  // compaction; longer rows are read from global memory on each pass
+  constexpr int KPT = 4096 / NT;
+  const bool cached = K <= static_cast<int64_t>(KPT) * NT;
+  uint32_t kreg[KPT];
+  if (cached) {
+#pragma unroll
+    for (int c = 0; c < KPT; ++c) {
+      const int64_t k = static_cast<int64_t>(c) * NT + threadIdx.x;
+      kreg[c] = k < K ? key[k] : 0u;
+    }
+  }
+
   uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(L);
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
     __syncthreads();
-    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
-      const uint32_t x = key[k];
-      if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+    if (cached) {
+#pragma unroll
+      for (int c = 0; c < KPT; ++c) {
+        const uint32_t x = kreg[c];
+        if (static_cast<int64_t>(c) * NT + threadIdx.x < K && (x & mask) == prefix)
+          atomicAdd(&hist[(x >> shift) & 255u], 1u);
+      }
+    } else {
+      for (int64_t k = threadIdx.x; k < K; k += NT) {
+        const uint32_t x = key[k];
+        if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+      }
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -188,9 +210,7 @@ __global__ void __launch_bounds__(NT) k_tw_select(const float* __restrict__ scor
   // block scan of both counts (16 bits each) per 1024 keys.
   const uint32_t thr = prefix, take_eq = remaining;
   uint32_t gt_base = 0, eq_base = 0;
-  for (int64_t k0 = 0; k0 < K; k0 += blockDim.x) {
-    const int64_t k = k0 + threadIdx.x;
-    const uint32_t x = (k < K) ? key[k] : 0u;
+  auto compact = [&](uint32_t x, int64_t k) {  // every thread, once per NT keys
     const uint32_t gt = (k < K && x > thr) ? 1u : 0u;
     const uint32_t eq = (k < K && x == thr) ? 1u : 0u;
     uint32_t total;
@@ -201,6 +221,18 @@ __global__ void __launch_bounds__(NT) k_tw_select(const float* __restrict__ scor
     if (take && pos < static_cast<uint32_t>(L)) out[pos] = static_cast<int32_t>(k);
     gt_base += total & 0xFFFFu;
     eq_base += total >> 16;
+  };
+  if (cached) {
+#pragma unroll
+    for (int c = 0; c < KPT; ++c) {
+      if (static_cast<int64_t>(c) * NT >= K) break;  // uniform over the block
+      compact(kreg[c], static_cast<int64_t>(c) * NT + threadIdx.x);
+    }
+  } else {
+    for (int64_t k0 = 0; k0 < K; k0 += NT) {
+      const int64_t k = k0 + threadIdx.x;
+      compact(k < K ? key[k] : 0u, k);
+    }
   }
 }
 
