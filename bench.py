@@ -706,7 +706,7 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-PROFILE_CASES = ("headline", "headline_bf16", "compress", "tvw", "tw", "tw_prune", "dense_4096")
+PROFILE_CASES = ("headline", "headline_bf16", "compress", "tvw", "tw", "tw_prune", "dense_4096", "ew")
 
 
 def run_profile_case(case: str) -> None:
@@ -737,6 +737,9 @@ def run_profile_case(case: str) -> None:
             fn = lambda: ss.tw_prune_compress(Wt, keep4, True, work, out=form)
         elif case == "dense_4096":
             fn = lambda: ss.dense_gemm(Wt, Xt, out=Yt)
+        elif case == "ew":  # the element-wise SpMM at 90 % sparsity
+            form = ss.ew_prune_compress(Wt, round(0.1 * tw.K))
+            fn = lambda: ss.ew_spmm(form, Xt, out=Yt)
         else:
             form = ss.tw_prune_compress(Wt, keep4 if case == "tvw" else keep, case == "tvw", work)
             fn = lambda: ss.tvw_gemm(form, Xt, out=Yt)

@@ -16,10 +16,11 @@
 //   k_ew_values  the kept values' stored bits (k_ew_row_ptr: the row pointers);
 //   k_ew_spmm    one CTA per (32 rows, 256 columns), three per SM: the X panel
 //                streams through shared memory in 64-row chunks (double-buffered
-//                cp.async); each warp owns 4 rows and, for every kept entry of a row that falls in
-//                the chunk, adds w times the chunk's X row into 8 fp32 accumulators
-//                per lane (the entries of a row are held 32 at a time in registers,
-//                one per lane, and broadcast by shuffles).
+//                cp.async); each warp owns 4 rows and, for every kept entry of a row
+//                that falls in the chunk, adds w times the chunk's X row into 8 fp32
+//                accumulators per lane, held and updated as packed pairs (the entries
+//                of a row are held 32 at a time in registers, one per lane, and
+//                broadcast by one shuffle of the entry's chunk row and value bits).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -106,11 +107,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
   int32_t used[kRowsW];  // entries of the current batch already consumed
 #pragma unroll
   for (int r = 0; r < kRowsW; ++r) used[r] = 0;
-  float acc[kRowsW][8];
+  // fp32 accumulators as packed pairs: acc[r][h] holds columns 2h (low word) and 2h + 1
+  uint64_t acc[kRowsW][4];
 #pragma unroll
   for (int r = 0; r < kRowsW; ++r)
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+    for (int h = 0; h < 4; ++h) acc[r][h] = 0ull;
 
   // chunk loader: 64 rows x 256 columns (32 KB) by 16-byte cp.async, zero past K / N
   auto load_chunk = [&](int64_t c, int buf) {
@@ -148,18 +150,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
       while (true) {
         const uint32_t in_chunk = __ballot_sync(0xffffffffu, bcol[r] < kend);
         const int n = __popc(in_chunk);
+        // each lane's entry as one word: the row of the chunk (a CSR whose columns are
+        // not ascending breaks the contract; such an entry gets an offset past the
+        // chunk and is skipped rather than read outside it) and the value's bits
+        const uint32_t off = static_cast<uint32_t>(bcol[r] - kbase);
+        const uint32_t ent = ((off < static_cast<uint32_t>(kChunk) ? off : 0xFFFFu) << 16) | (bval[r] & 0xFFFFu);
         for (int e = used[r]; e < n; ++e) {
-          const int32_t col = __shfl_sync(0xffffffffu, bcol[r], e);
-          const float w = to_f32<DT>(__shfl_sync(0xffffffffu, bval[r], e));
-          // a CSR whose columns are not ascending breaks the contract; such an entry is
-          // skipped rather than read outside the chunk
-          if (static_cast<uint32_t>(col - kbase) >= static_cast<uint32_t>(kChunk)) continue;
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (col - kbase) * (kCols * 2));
+          const uint32_t en = __shfl_sync(0xffffffffu, ent, e);
+          if ((en >> 16) >= static_cast<uint32_t>(kChunk)) continue;
+          const float w = to_f32<DT>(en & 0xFFFFu);
+          const uint64_t w2 = ptx::f2_pack(w, w);
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (en >> 16) * (kCols * 2));
           const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            acc[r][2 * h] = fmaf(w, to_f32<DT>(xw[h] & 0xFFFFu), acc[r][2 * h]);
-            acc[r][2 * h + 1] = fmaf(w, to_f32<DT>(xw[h] >> 16), acc[r][2 * h + 1]);
+            // the pair of X values as fp32 (bf16: the upper halves of two words)
+            const uint64_t x2 =
+                DT == 1 ? ptx::f2_pack(__uint_as_float(xw[h] << 16), __uint_as_float(xw[h] & 0xFFFF0000u))
+                        : ptx::f2_pack(to_f32<DT>(xw[h] & 0xFFFFu), to_f32<DT>(xw[h] >> 16));
+            acc[r][h] = ptx::f2_fma(w2, x2, acc[r][h]);
           }
         }
         used[r] = n;
@@ -185,10 +194,10 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       if constexpr (DT == 1) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[r][2 * h], acc[r][2 * h + 1]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(ptx::f2_lo(acc[r][h]), ptx::f2_hi(acc[r][h]));
         w[h] = *reinterpret_cast<const uint32_t*>(&b);
       } else {
-        const __half2 b = __floats2half2_rn(acc[r][2 * h], acc[r][2 * h + 1]);
+        const __half2 b = __floats2half2_rn(ptx::f2_lo(acc[r][h]), ptx::f2_hi(acc[r][h]));
         w[h] = *reinterpret_cast<const uint32_t*>(&b);
       }
     }
