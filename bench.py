@@ -709,7 +709,8 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-PROFILE_CASES = ("headline", "headline_bf16", "compress", "tvw", "tw", "tw_prune", "dense_4096", "ew")
+PROFILE_CASES = ("headline", "headline_bf16", "compress", "tvw", "tw", "tw_prune", "dense_4096", "ew", "bw",
+                 "conv_tw")
 
 
 def run_profile_case(case: str) -> None:
@@ -743,6 +744,17 @@ def run_profile_case(case: str) -> None:
         elif case == "ew":  # the element-wise SpMM at 90 % sparsity
             form = ss.ew_prune_compress(Wt, round(0.1 * tw.K))
             fn = lambda: ss.ew_spmm(form, Xt, out=Yt)
+        elif case == "bw":  # block-wise at the tile-wise kept fractions (64-column blocks)
+            form = ss.bw_prune_compress(Wt, (keep // 64).astype(np.int32))
+            fn = lambda: ss.bw_gemm(form, Xt, out=Yt)
+        elif case == "conv_tw":  # ResNet-50 28 x 28 x 128 -> 128 3x3, batch 32, tile-wise filter
+            g = np.random.default_rng(7)
+            Xc = torch.from_numpy(g.standard_normal((32, 28, 28, 128)).astype(np.float32)).to(dev, torch.bfloat16)
+            Wc = torch.from_numpy((g.standard_normal((128, 9 * 128)) * (2.0 / (9 * 128)) ** 0.5).astype(np.float32)
+                                  ).to(dev, torch.bfloat16)
+            form = ss.bw_prune_compress(Wc, np.full(1, round(0.25 * 9 * 128 // 64), dtype=np.int32))
+            Yc = torch.empty((128, 32 * 28 * 28), dtype=torch.bfloat16, device=dev)
+            fn = lambda: ss.conv3x3(form, Xc, out=Yc)
         else:
             form = ss.tw_prune_compress(Wt, keep4 if case == "tvw" else keep, case == "tvw", work)
             fn = lambda: ss.tvw_gemm(form, Xt, out=Yt)
