@@ -155,12 +155,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
         // chunk and is skipped rather than read outside it) and the value's bits
         const uint32_t off = static_cast<uint32_t>(bcol[r] - kbase);
         const uint32_t ent = ((off < static_cast<uint32_t>(kChunk) ? off : 0xFFFFu) << 16) | (bval[r] & 0xFFFFu);
-        for (int e = used[r]; e < n; ++e) {
-          const uint32_t en = __shfl_sync(0xffffffffu, ent, e);
-          if ((en >> 16) >= static_cast<uint32_t>(kChunk)) continue;
+        // w times the X row of entry en (entries past the chunk add nothing)
+        auto add_entry = [&](uint32_t en) {
+          const bool ok = (en >> 16) < static_cast<uint32_t>(kChunk);
           const float w = to_f32<DT>(en & 0xFFFFu);
           const uint64_t w2 = ptx::f2_pack(w, w);
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (en >> 16) * (kCols * 2));
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (ok ? (en >> 16) : 0u) * (kCols * 2));
           const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -168,9 +168,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
             const uint64_t x2 =
                 DT == 1 ? ptx::f2_pack(__uint_as_float(xw[h] << 16), __uint_as_float(xw[h] & 0xFFFF0000u))
                         : ptx::f2_pack(to_f32<DT>(xw[h] & 0xFFFFu), to_f32<DT>(xw[h] >> 16));
-            acc[r][h] = ptx::f2_fma(w2, x2, acc[r][h]);
+            if (ok) acc[r][h] = ptx::f2_fma(w2, x2, acc[r][h]);
           }
+        };
+        // two entries a turn, so that their shuffles and shared-memory reads overlap
+        int e = used[r];
+        for (; e + 1 < n; e += 2) {
+          const uint32_t en0 = __shfl_sync(0xffffffffu, ent, e), en1 = __shfl_sync(0xffffffffu, ent, e + 1);
+          add_entry(en0);
+          add_entry(en1);
         }
+        if (e < n) add_entry(__shfl_sync(0xffffffffu, ent, e));
         used[r] = n;
         if (n < 32 || pos[r] + 32 >= end[r]) break;  // the batch reaches past this chunk, or the row ends
         // the whole batch was inside the chunk: fetch the next 32 entries
