@@ -155,3 +155,46 @@ def test_llm_ffn_e4m3_epilogue_sampled_rows():
     yr = bits_of(Y.view(torch.uint8)[torch.from_numpy(rows).cuda()])
     ok = oracle.epilogue.within_bound_ep(yr, ref, B, "e4m3", REL["e4m3"], "gelu", 8.0)
     assert ok.all(), f"{(~ok).sum()} outside the bound"
+
+
+@pytest.mark.parametrize("out_dt", ["bf16", "e4m3"])
+@pytest.mark.parametrize("tile", [0, 19256])
+def test_gelu_at_chosen_values(out_dt, tile):
+    """GELU through the GEMM on chosen inputs: a 2:4 identity weight makes each
+    accumulator exactly one X value (zero, tiny, moderate, large and far into either
+    tail, both signs), with and without a bias. The accumulator is exact here, so the
+    result must be the oracle's exact GELU to within the kernel's erf approximation
+    (Abramowitz-Stegun 7.1.26: GELU error <= 1.7e-7 max(|x|, 1), absolute; relative to
+    the tiny values of the far negative tail that is several output ulps) and one
+    output ulp."""
+    ss = lib()
+    K = N = 256
+    M = 256
+    W = np.zeros((M, K))
+    W[np.arange(M), np.arange(M) % K] = 1.0
+    Wb = oracle.codecs.encode(W, "bf16")
+    vals = np.array([0.0, -0.0, 1e-30, -1e-30, 1e-3, -1e-3, 0.25, -0.25, 0.5, -0.5, 1.0, -1.0, 1.5, -1.5, 2.0, -2.0,
+                     3.0, -3.0, 4.5, -4.5, 5.5, -5.5, 8.0, -8.0, 12.0, -12.0, 20.0, -20.0, 100.0, -100.0, 1e4, -1e4])
+    X = np.tile(vals, (K, N // len(vals)))
+    X = X * (1.0 + np.arange(K)[:, None] / K)              # a different scale per row of X
+    Xb = oracle.codecs.encode(X, "bf16")
+    bias = np.where(np.arange(M) % 3 == 0, 0.0, np.where(np.arange(M) % 3 == 1, 2.0, -2.0)).astype(np.float32)
+    ys = 4.0 if out_dt == "e4m3" else 1.0
+    f = ss.sp24_prune_compress(dev_tensor(Wb, "bf16"), canonical_meta=False)
+    Y, buf = guarded_output(M, N, TORCH_OUT[out_dt], pad_cols=16)  # row pitch a multiple of 16 bytes
+    ss.sp24_gemm(f, dev_padded(Xb, "bf16"), out=Y, bias=torch.from_numpy(bias).cuda(), act="gelu", y_scale=ys,
+                 variant=tile)
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
+    acc = oracle.codecs.decode(Wb, "bf16") @ oracle.codecs.decode(Xb, "bf16")
+    z = acc + bias.astype(np.float64)[:, None]
+    want = oracle.codecs.encode(oracle.epilogue.apply(acc, bias.astype(np.float64), "gelu", ys), out_dt)
+    y = oracle.codecs.decode(bits_of(Y), out_dt)
+    r = oracle.codecs.decode(want, out_dt)
+    slack = ys * 1.7e-7 * np.maximum(np.abs(z), 1.0) + oracle.epilogue.ulp(np.maximum(np.abs(y), np.abs(r)), out_dt)
+    bad = ~((np.abs(y - r) <= slack) & np.isfinite(y))
+    assert not bad.any(), f"{bad.sum()} off; first at z = {z[bad][0]}: gpu {y[bad][0]} ref {r[bad][0]}"
+    # inside |z| <= 3 the approximation is far below half an ulp: one ulp at most
+    near = np.abs(z) <= 3.0
+    assert (np.abs(y - r)[near] <= oracle.epilogue.ulp(np.maximum(np.abs(y), np.abs(r)), out_dt)[near]).all()
+    assert canary_intact(buf, M, N)
