@@ -505,9 +505,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
             if (KX == 2 && leader) ptx::mbar_arrive_expect_tx(&full_b[stage], 2u * C::B_BYTES);
             const uint32_t bar = ptx::mapa(ptx::smem_u32(&full[stage]), crank & ~1u);
             const uint32_t bar_b = KX == 2 ? ptx::mapa(ptx::smem_u32(&full_b[stage]), crank & ~1u) : bar;
-            ptx::tma_load_2d_pair(sA, &tmA, bar, kb * (SPARSE ? C::BK / 2 : C::BK), ui.m0, pol_a);
-            if constexpr (SPARSE)  // one metadata block; past the last row block it reads zeros
-              ptx::tma_load_2d_pair(sM, &tmM, bar, 0, (ui.meta_blk0 + KX * kb) * 16, pol_a);
+            // the X panel, the stage's largest copy, first
             const int32_t n_half = ui.n0 + static_cast<int32_t>(crank & 1u) * C::BN_CTA;
             if (C::B_BOXES > 1 && p.b3d) {
               // all of this CTA's B boxes of the stage as one 3-D box: the layout
@@ -519,6 +517,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
                 ptx::tma_load_2d_pair(sB + bx * C::B_BOX_BYTES, &tmB, bar_b, n_half + bx * C::B_BOX_COLS,
                                       kb * C::BK, pol_b);
             }
+            ptx::tma_load_2d_pair(sA, &tmA, bar, kb * (SPARSE ? C::BK / 2 : C::BK), ui.m0, pol_a);
+            if constexpr (SPARSE)  // one metadata block; past the last row block it reads zeros
+              ptx::tma_load_2d_pair(sM, &tmM, bar, 0, (ui.meta_blk0 + KX * kb) * 16, pol_a);
           } else {
           // 2:4 metadata blocks of the stage (KX per sub-tile; the last stage of a row
           // block may cover only one of two)
