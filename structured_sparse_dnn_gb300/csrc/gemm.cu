@@ -526,19 +526,7 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           const int32_t meta_n = SPARSE ? min(KX, p.meta_kb - KX * kb) : 0;
           ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0u : (CONV ? p.conv_box_bytes : C::B_BYTES)) +
                                                        static_cast<uint32_t>(2048 * meta_n * ui.subs));
-          // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
-          // rows past M read as zeros
-          const int32_t a_col = C::SCHEDULED ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
-          const int32_t a_row = C::SCHEDULED ? ui.a_row0 + 128 * kb : ui.m0;
-          ptx::tma_load_2d(sA, &tmA, &full[stage], a_col, a_row, pol_a);
-          if constexpr (SPARSE) {
-            for (int mt = 0; mt < ui.subs; ++mt) {
-              // sub-tile mt's blocks follow the row block's meta_kb blocks (TW/TVW tiles: nk)
-              const int32_t stride = C::SCHEDULED ? ui.nk : p.meta_kb;
-              const uint8_t* src = p.meta_hw + static_cast<int64_t>(ui.meta_blk0 + mt * stride + KX * kb) * 2048;
-              ptx::bulk_load(sM + mt * 2048 * KX, src, static_cast<uint32_t>(2048 * meta_n), &full[stage], pol_a);
-            }
-          }
+          // the X operand first (the stage's largest copy), then A and the metadata
           if constexpr (CONV) {
             // tap (r, s) and 64 input channels of K stage kb, for the patch's image rows
             // shifted by the tap (out-of-range rows and columns read as zeros)
@@ -555,6 +543,19 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
             for (int bx = 0; bx < C::B_BOXES; ++bx)
               ptx::tma_load_2d(sB + bx * C::B_BOX_BYTES, &tmB, &full[stage], ui.n0 + bx * C::B_BOX_COLS, krow,
                                pol_b);
+          }
+          // A: dense W / 2:4 values / packed tile box (inner coordinate in elements);
+          // rows past M read as zeros
+          const int32_t a_col = C::SCHEDULED ? 0 : kb * (SPARSE ? C::BK / 2 : C::BK);
+          const int32_t a_row = C::SCHEDULED ? ui.a_row0 + 128 * kb : ui.m0;
+          ptx::tma_load_2d(sA, &tmA, &full[stage], a_col, a_row, pol_a);
+          if constexpr (SPARSE) {
+            for (int mt = 0; mt < ui.subs; ++mt) {
+              // sub-tile mt's blocks follow the row block's meta_kb blocks (TW/TVW tiles: nk)
+              const int32_t stride = C::SCHEDULED ? ui.nk : p.meta_kb;
+              const uint8_t* src = p.meta_hw + static_cast<int64_t>(ui.meta_blk0 + mt * stride + KX * kb) * 2048;
+              ptx::bulk_load(sM + mt * 2048 * KX, src, static_cast<uint32_t>(2048 * meta_n), &full[stage], pol_a);
+            }
           }
           }
         }
