@@ -186,6 +186,40 @@ def pct(xs, q: float) -> float:
     return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
 
 
+def graph_ms(body, n: int, side) -> float:
+    """ms per call of `body`: n calls captured in one CUDA graph on stream `side`,
+    replayed three times after three untimed replays, best of the three."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        body()                                         # first call outside capture (library set-up)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+            for _ in range(n):
+                body()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(side)
+        with torch.cuda.stream(side):
+            g.replay()
+        b.record(side)
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del g
+    return best / n
+
+
+def flushed_graph_ms(fn, flush: torch.Tensor, dev, n: int = 20) -> float:
+    """ms per call of `fn` with L2 flushed before each: n (flush, call) pairs in one
+    graph minus n flushes alone (launch latency amortised)."""
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    return graph_ms(lambda: (flush.fill_(1), fn()), n, side) - graph_ms(lambda: flush.fill_(1), n, side)
+
+
 def headline_protocol(step, flush, stream, dev, eff_flops) -> dict:
     """The headline kernel under three timings: 50 eager launches each after an L2
     flush (CUDA events around each: p10 / median / p90); 50 launches replayed from one
@@ -196,32 +230,9 @@ def headline_protocol(step, flush, stream, dev, eff_flops) -> dict:
     side = torch.cuda.Stream(device=dev)
     side.wait_stream(torch.cuda.current_stream(dev))
 
-    def graph_ms(body) -> float:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(side):
-            body()                                         # first call outside capture (library set-up)
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
-                for _ in range(n):
-                    body()
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        best = float("inf")
-        for _ in range(3):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(side)
-            with torch.cuda.stream(side):
-                g.replay()
-            b.record(side)
-            torch.cuda.synchronize()
-            best = min(best, a.elapsed_time(b))
-        del g
-        return best / n
-
-    warm = graph_ms(step)
-    with_flush = graph_ms(lambda: (flush.fill_(1), step()))
-    flush_only = graph_ms(lambda: flush.fill_(1))
+    warm = graph_ms(step, n, side)
+    with_flush = graph_ms(lambda: (flush.fill_(1), step()), n, side)
+    flush_only = graph_ms(lambda: flush.fill_(1), n, side)
     cold = with_flush - flush_only
     tf = lambda ms: round(eff_flops / (ms * 1e-3) / 1e12, 1)
     return {"eager_l2_flushed": {"launches": n, "p10_ms": round(pct(eager, 10), 5),
@@ -457,10 +468,16 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
     eb = I.ELEM_BYTES[wl.dt]
     vb, mb, hb = ss.sp24_sizes(ss._DT[Wd.dtype], M, K)
     # a1: prune + compress (HBM bound): read W, write values + operand-order metadata
-    t = statistics.mean(timed_steps(lambda: ss.sp24_prune_compress(Wd, canonical_meta=False), steps, 2, flush, stream))
+    compress = lambda: ss.sp24_prune_compress(Wd, canonical_meta=False)
+    t = statistics.mean(timed_steps(compress, steps, 2, flush, stream))
+    tg = flushed_graph_ms(compress, flush, dev)
     nbytes = M * K * eb + vb + hb
     rows["sp24_prune_compress"] = {"workload": wl.name, "ms": round(t, 4), "GB/s": round(nbytes / t / 1e6, 1),
-                                   "frac_of_hbm": round(nbytes / t / 1e6 / pk["hbm_gbs"], 3)}
+                                   "frac_of_hbm": round(nbytes / t / 1e6 / pk["hbm_gbs"], 3),
+                                   "graph_l2_flushed": {"ms": round(tg, 4), "GB/s": round(nbytes / tg / 1e6, 1),
+                                                        "frac_of_hbm": round(nbytes / tg / 1e6 / pk["hbm_gbs"], 3),
+                                                        "note": "20 (L2 flush, call) pairs in one graph minus 20 "
+                                                                "flushes alone"}}
     # a8: the dense GEMM of the same kernel family on the same shape
     Yd = torch.empty((M, N), dtype=torch.bfloat16 if wl.out_dt == "bf16" else torch.float16, device=dev)
     t = statistics.mean(timed_steps(lambda: ss.dense_gemm(Wd, Xd, alpha=d["alpha"], out=Yd), steps, 2, flush,
@@ -508,27 +525,9 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
         Ys = torch.empty((ws.M, ws.N), dtype=Ws.dtype, device=dev)
         t_cold = statistics.median(timed_steps(lambda: ss.sp24_gemm(fs, Xs, out=Ys), steps, 3, flush, stream))
         t_dense = statistics.median(timed_steps(lambda: ss.dense_gemm(Ws, Xs, out=Ys), steps, 3, flush, stream))
-        reps = 20
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(side):
-            ss.sp24_gemm(fs, Xs, out=Ys)          # first call outside capture (library set-up)
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
-                for _ in range(reps):
-                    ss.sp24_gemm(fs, Xs, out=Ys)
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(side)
-        with torch.cuda.stream(side):
-            for _ in range(5):
-                g.replay()
-        b.record(side)
-        torch.cuda.synchronize()
-        t_warm = a.elapsed_time(b) / (5 * reps)
+        t_warm = graph_ms(lambda: ss.sp24_gemm(fs, Xs, out=Ys), 20, side)
         vb_s, _, hb_s = ss.sp24_sizes(ss._DT[Ws.dtype], ws.M, ws.K)
         nbytes = vb_s + hb_s + ws.K * ws.N * 2 + ws.M * ws.N * 2
         small[name] = {"MxNxK": f"{ws.M}x{ws.N}x{ws.K}", "us_l2_flushed": round(t_cold * 1e3, 2),
@@ -536,7 +535,7 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
                        "us_graph_back_to_back": round(t_warm * 1e3, 2),
                        "effective_TFLOP/s_graph": round(ws.M * ws.N * ws.K / (t_warm * 1e-3) / 1e12, 1),
                        "GB/s_graph": round(nbytes / (t_warm * 1e-3) / 1e9, 1)}
-        del dsm, Ws, Xs, fs, Ys, g
+        del dsm, Ws, Xs, fs, Ys
     rows["sp24_gemm_small_configs"] = small
     # a3-a7: tile-wise prune and the TW / TVW gather GEMMs vs the same-kernel dense GEMM
     tw = I.WORKLOADS["tile_wise_4096_bf16"]
@@ -710,7 +709,7 @@ def run_reference(args) -> None:
 
 
 PROFILE_CASES = ("headline", "headline_bf16", "compress", "tvw", "tw", "tw_prune", "dense_4096", "ew", "bw",
-                 "conv_tw")
+                 "conv_tw", "conv_sp24")
 
 
 def run_profile_case(case: str) -> None:
@@ -726,6 +725,20 @@ def run_profile_case(case: str) -> None:
         Y = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device=dev)
         fn = ((lambda: ss.sp24_prune_compress(Wd, canonical_meta=False)) if case == "compress"
               else (lambda: ss.sp24_gemm(form, Xd, alpha=d["alpha"], out=Y)))
+    elif case in ("conv_tw", "conv_sp24"):
+        # ResNet-50 3x3 layers, batch 32: 28 x 28 x 128 -> 128 with the tile-wise filter (a
+        # quarter of the (tap, 64-channel) groups), 14 x 14 x 256 -> 256 with the 2:4 filter
+        H, Cin, Cout = (28, 128, 128) if case == "conv_tw" else (14, 256, 256)
+        g = np.random.default_rng(7)
+        Xc = torch.from_numpy(g.standard_normal((32, H, H, Cin)).astype(np.float32)).to(dev, torch.bfloat16)
+        Wc = torch.from_numpy((g.standard_normal((Cout, 9 * Cin)) * (2.0 / (9 * Cin)) ** 0.5).astype(np.float32)
+                              ).to(dev, torch.bfloat16)
+        if case == "conv_tw":
+            form = ss.bw_prune_compress(Wc, np.full((Cout + 127) // 128, round(0.25 * 9 * Cin // 64), dtype=np.int32))
+        else:
+            form = ss.sp24_prune_compress(Wc, canonical_meta=False)
+        Yc = torch.empty((Cout, 32 * H * H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: ss.conv3x3(form, Xc, out=Yc)
     else:
         tw = I.WORKLOADS["tile_wise_4096_bf16"]
         d = tw.make()
@@ -747,14 +760,6 @@ def run_profile_case(case: str) -> None:
         elif case == "bw":  # block-wise at the tile-wise kept fractions (64-column blocks)
             form = ss.bw_prune_compress(Wt, (keep // 64).astype(np.int32))
             fn = lambda: ss.bw_gemm(form, Xt, out=Yt)
-        elif case == "conv_tw":  # ResNet-50 28 x 28 x 128 -> 128 3x3, batch 32, tile-wise filter
-            g = np.random.default_rng(7)
-            Xc = torch.from_numpy(g.standard_normal((32, 28, 28, 128)).astype(np.float32)).to(dev, torch.bfloat16)
-            Wc = torch.from_numpy((g.standard_normal((128, 9 * 128)) * (2.0 / (9 * 128)) ** 0.5).astype(np.float32)
-                                  ).to(dev, torch.bfloat16)
-            form = ss.bw_prune_compress(Wc, np.full(1, round(0.25 * 9 * 128 // 64), dtype=np.int32))
-            Yc = torch.empty((128, 32 * 28 * 28), dtype=torch.bfloat16, device=dev)
-            fn = lambda: ss.conv3x3(form, Xc, out=Yc)
         else:
             form = ss.tw_prune_compress(Wt, keep4 if case == "tvw" else keep, case == "tvw", work)
             fn = lambda: ss.tvw_gemm(form, Xt, out=Yt)

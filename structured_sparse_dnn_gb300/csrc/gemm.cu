@@ -164,8 +164,8 @@ struct Cfg {
   static_assert(!CONV || (!GATHER && !PAIR && MT == 1 && Elem<DT>::bytes == 2),
                 "convolution: 16-bit, 128-row tiles");
   static_assert(META_COL0 + META_COLS <= 512, "accumulators and metadata exceed TMEM");
-  static_assert(KX == 1 || (KX == 2 && SPARSE && MT == 1 && !GATHER && !CONV && !BLOCKW),
-                "double K stages: 2:4 tiles of 128 rows (one CTA or an SM pair)");
+  static_assert(KX == 1 || (KX == 2 && SPARSE && MT == 1 && !GATHER && !BLOCKW),
+                "double K stages: 2:4 tiles of 128 rows (one CTA, an SM pair or a convolution)");
   // SM pairs with two-step stages take their X boxes on a second barrier
   static constexpr bool B_OWN_BARRIER = PAIR && KX == 2;
   static_assert(MT == 1 || !GATHER, "256-row tiles: no gather");
@@ -225,7 +225,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const Params& p, int32_t u, uint
     ui.m0 = mb * 128;
     ui.n0 = (ui.img * p.conv_h + ui.h0) * p.conv_w;
     ui.ncols = min(p.conv_rows, p.conv_h - ui.h0) * p.conv_w;
-    ui.meta_blk0 = mb * p.nk;
+    ui.meta_blk0 = mb * p.meta_kb;
     ui.subs = 1;
     return ui;
   }
@@ -379,6 +379,64 @@ __device__ __forceinline__ void store_packed_row32(uint8_t* dst_row, int32_t n0,
   }
 }
 
+// The same for the output of a convolution unit, whose columns start at any
+// offset of the row (patches of W-wide image rows).
+__device__ __forceinline__ void store_packed_row32_any(uint8_t* dst_row, int32_t n0, int32_t N, int out_dt,
+                                                       const uint32_t (&w)[16], uint64_t pol) {
+  if (out_dt == 2) {
+    uint8_t* dst = dst_row + n0;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+    if (n0 + 32 <= N && (a & 15u) == 0) {
+      ptx::st_global_v4_hint(dst, w[0], w[1], w[2], w[3], pol);
+      ptx::st_global_v4_hint(dst + 16, w[4], w[5], w[6], w[7], pol);
+    } else if (n0 + 32 <= N && (a & 3u) == 0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) reinterpret_cast<uint32_t*>(dst)[k] = w[k];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < N) dst[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+    }
+    return;
+  }
+  uint16_t* dst = reinterpret_cast<uint16_t*>(dst_row) + n0;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+  if (n0 + 32 <= N && (a & 15u) == 0) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      ptx::st_global_v4_hint(reinterpret_cast<uint4*>(dst) + v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3],
+                             pol);
+    return;
+  }
+  // A column range at another offset (convolution patches of W-wide image rows, a
+  // ragged row end): element pairs as 32-bit stores from the first 4-byte boundary
+  // on, with a 2-byte store at either end where needed (n0 < N, so cnt >= 1).
+  const int32_t cnt = min(32, N - n0);
+  if (cnt == 32 && (a & 7u) == 0) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) reinterpret_cast<uint2*>(dst)[k] = make_uint2(w[2 * k], w[2 * k + 1]);
+  } else if ((a & 2u) == 0) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (2 * k + 1 < cnt)
+        reinterpret_cast<uint32_t*>(dst)[k] = w[k];
+      else if (2 * k < cnt)
+        dst[2 * k] = static_cast<uint16_t>(w[k]);
+    }
+  } else {
+    dst[0] = static_cast<uint16_t>(w[0]);
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + 1);  // elements 2k + 1 and 2k + 2
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t lo = w[k] >> 16, hi = k < 15 ? (w[k + 1] & 0xFFFFu) : 0u;
+      if (2 * k + 2 < cnt)
+        d32[k] = lo | (hi << 16);
+      else if (2 * k + 1 < cnt)
+        dst[2 * k + 1] = static_cast<uint16_t>(lo);
+    }
+  }
+}
+
 // Writes 32 packed outputs as row `lane` of a 32 x 32 staging box: 64-byte rows
 // with the 64B swizzle (fp16/bf16) or 32-byte rows with the 32B swizzle (e4m3),
 // the layouts the output tensor map stores from, without bank conflicts between
@@ -524,18 +582,23 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           // 2:4 metadata blocks of the stage (KX per sub-tile; the last stage of a row
           // block may cover only one of two)
           const int32_t meta_n = SPARSE ? min(KX, p.meta_kb - KX * kb) : 0;
-          ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + (GATHER ? 0u : (CONV ? p.conv_box_bytes : C::B_BYTES)) +
+          ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES +
+                                                       (GATHER ? 0u : (CONV ? KX * p.conv_box_bytes : C::B_BYTES)) +
                                                        static_cast<uint32_t>(2048 * meta_n * ui.subs));
           // the X operand first (the stage's largest copy), then A and the metadata
           if constexpr (CONV) {
-            // tap (r, s) and 64 input channels of K stage kb, for the patch's image rows
-            // shifted by the tap (out-of-range rows and columns read as zeros)
+            // tap (r, s) and 64 input channels of each K step of stage kb, for the patch's
+            // image rows shifted by the tap (out-of-range rows and columns read as zeros)
             // (tile-wise filter: the kb-th kept (tap, 64-channel) group of the tile)
             const int32_t cblocks = p.conv_cin / 64;
-            const int32_t g = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) : kb;
-            const int32_t tap = g / cblocks, c0 = (g - tap * cblocks) * 64;
-            const int32_t r = tap / 3, sx = tap - 3 * r;
-            ptx::tma_load_4d(sB, &tmB, &full[stage], c0, sx - 1, ui.h0 + r - 1, ui.img, pol_b);
+#pragma unroll
+            for (int x = 0; x < KX; ++x) {
+              const int32_t g = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) : KX * kb + x;
+              const int32_t tap = g / cblocks, c0 = (g - tap * cblocks) * 64;
+              const int32_t r = tap / 3, sx = tap - 3 * r;
+              ptx::tma_load_4d(sB + x * (C::B_BYTES / KX), &tmB, &full[stage], c0, sx - 1, ui.h0 + r - 1, ui.img,
+                               pol_b);
+            }
           } else if constexpr (!GATHER) {
             // block-wise: the X panel of the kb-th kept block of this tile
             const int32_t krow = BLOCKW ? __ldg(p.indices + ui.idx_base + kb) * C::BK : kb * C::BK;
@@ -634,8 +697,11 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           for (int mt = 0; mt < MT; ++mt) {
             const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
             // B: MN-major boxes, or (convolution) K-major pixel rows of 128 bytes
-            const uint64_t bdesc = CONV ? ptx::sdesc(sB + j * C::MMA_K * C::EB, 16, 1024, 2)
-                                        : ptx::sdesc(sB + j * C::MMA_K * C::B_ROW, C::B_BOX_BYTES, C::B_SBO, C::B_SWZ);
+            // (KX = 2: the stage's second K step in the second box)
+            constexpr int kJPS = C::MMAS / KX;  // instructions per K step
+            const uint64_t bdesc =
+                CONV ? ptx::sdesc(sB + (j / kJPS) * (C::B_BYTES / KX) + (j % kJPS) * C::MMA_K * C::EB, 16, 1024, 2)
+                     : ptx::sdesc(sB + j * C::MMA_K * C::B_ROW, C::B_BOX_BYTES, C::B_SBO, C::B_SWZ);
             const uint32_t d_sub = d_tmem + static_cast<uint32_t>(mt * BN);
             const uint32_t a_sub = sA + static_cast<uint32_t>(mt * C::A_SUB_BYTES);
             if constexpr (SPARSE) {
@@ -859,7 +925,10 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
           // convolution patches end at their last valid image row
           const int32_t n_lim = CONV ? ui.n0 + ui.ncols : p.N;
           if (!row_ok || n0 >= n_lim) return;
-          store_packed_row32(yrow, n0, n_lim, p.out_dt, w, pol_y);
+          if constexpr (CONV)
+            store_packed_row32_any(yrow, n0, n_lim, p.out_dt, w, pol_y);
+          else
+            store_packed_row32(yrow, n0, n_lim, p.out_dt, w, pol_y);
         }
       };
       if constexpr (C::EARLY_RELEASE) {
@@ -1007,6 +1076,9 @@ cudaError_t run(const GemmArgs& a, cudaStream_t s, uint32_t* err) {
     conv_rows = static_cast<int32_t>(BN / a.conv_w);
     if constexpr (BLOCKW)  // tile-wise filter: the packed kept groups seen as (packed_rows x 64)
       ok = make_map(&tA, a.A, eb, 64, a.packed_rows, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    else if constexpr (SPARSE && KX == 2)  // two K steps: 128-byte rows of compressed values
+      ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 128 / eb, C::BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
     else if constexpr (SPARSE)
       ok = make_map(&tA, a.A, eb, static_cast<uint64_t>(a.K / 2), a.M, a.lda * eb, 64 / eb, C::BM,
                     CU_TENSOR_MAP_SWIZZLE_64B);
@@ -1259,17 +1331,25 @@ cudaError_t dispatch_dt(int mode, const GemmArgs& a, cudaStream_t s, uint32_t* e
     return sparse ? run<DT, true, false, 256>(a, s, err) : run<DT, false, false, 256>(a, s, err);
   }
   if (mode == 5 || mode == 6 || mode == 7) {
-    // 3x3 convolution: N tiles of whole image rows, 224 columns (128 when that leaves
-    // fewer than two tiles per SM)
+    // 3x3 convolution: N tiles of whole image rows, 128 or 224 columns, whichever takes
+    // fewer rounds of units over the SMs, a 224-column unit costing about 1.35 times a
+    // 128-column one (measured on ResNet-50 layers, dense, 2:4 and tile-wise filters)
     if constexpr (EB == 2) {
-      const int64_t units224 = ceil_div(a.M, 128) * a.conv_nb * ceil_div(a.conv_h, 224 / a.conv_w);
-      const bool narrow_c = a.conv_w <= 128 && units224 < 2 * sm_count();
+      const int64_t sms = sm_count();
+      auto rounds = [&](int64_t bn) {
+        return ceil_div(ceil_div(a.M, 128) * a.conv_nb * ceil_div(a.conv_h, bn / a.conv_w), sms);
+      };
+      const bool narrow_c = a.conv_w <= 128 && 100 * rounds(128) < 135 * rounds(224);
       if (mode == 7)  // tile-wise filter
         return narrow_c ? run<DT, false, false, 128, 1, 128, false, true, true>(a, s, err)
                         : run<DT, false, false, 224, 1, 128, false, true, true>(a, s, err);
-      if (mode == 5)
+      if (mode == 5) {
+        // 128-column tiles over whole 128-channel K pairs: two K steps per stage
+        if (narrow_c && a.conv_cin % 128 == 0)
+          return run<DT, true, false, 128, 1, 128, false, false, true, 2>(a, s, err);
         return narrow_c ? run<DT, true, false, 128, 1, 128, false, false, true>(a, s, err)
                         : run<DT, true, false, 224, 1, 128, false, false, true>(a, s, err);
+      }
       return narrow_c ? run<DT, false, false, 128, 1, 128, false, false, true>(a, s, err)
                       : run<DT, false, false, 224, 1, 128, false, false, true>(a, s, err);
     }

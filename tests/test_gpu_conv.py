@@ -1,7 +1,8 @@
 """GPU parity of the 3x3 convolution (implicit GEMM, stride 1, zero padding)
 through the C ABI, with a 2:4 and a dense filter, against the oracle's im2col
 convolution: small and ragged images (H not a multiple of the row patch, C_out
-not a multiple of 128), both N tile widths, and the ResNet-50 stage-3 shape."""
+not a multiple of 128), both N tile widths, one and two K steps per stage, and the
+ResNet-50 layers of the benchmark."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +13,12 @@ from gpu_helpers import REL, bits_of, canary_intact, dev_tensor, guarded_output,
 pytestmark = pytest.mark.gpu
 
 # (Nb, H, W, Cin, Cout)
-CASES = [(1, 5, 7, 64, 128), (2, 14, 14, 128, 256), (1, 28, 28, 64, 200), (3, 9, 30, 64, 64), (1, 3, 224, 64, 128)]
+# (C_in a multiple of 128 with 128-column tiles: the 2:4 filter's stages carry two K steps;
+# odd image widths put a unit's first output column at an odd offset; the last two are the
+# ResNet-50 layers of the benchmark at its batch of 32)
+CASES = [(1, 5, 7, 64, 128), (2, 14, 14, 128, 256), (1, 28, 28, 64, 200), (3, 9, 30, 64, 64), (1, 3, 224, 64, 128),
+         (1, 28, 28, 128, 200), (2, 9, 30, 256, 64), (3, 7, 7, 128, 128), (1, 11, 13, 64, 64),
+         (32, 28, 28, 128, 128), (32, 14, 14, 256, 256)]
 
 
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
