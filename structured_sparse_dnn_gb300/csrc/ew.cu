@@ -150,17 +150,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
       while (true) {
         const uint32_t in_chunk = __ballot_sync(0xffffffffu, bcol[r] < kend);
         const int n = __popc(in_chunk);
-        // each lane's entry as one word: the row of the chunk (a CSR whose columns are
-        // not ascending breaks the contract; such an entry gets an offset past the
-        // chunk and is skipped rather than read outside it) and the value's bits
-        const uint32_t off = static_cast<uint32_t>(bcol[r] - kbase);
-        const uint32_t ent = ((off < static_cast<uint32_t>(kChunk) ? off : 0xFFFFu) << 16) | (bval[r] & 0xFFFFu);
-        // w times the X row of entry en (entries past the chunk add nothing)
+        // each lane's entry as one word: the row of the chunk and the value's bits. The
+        // row is clamped to the chunk: under the contract (ascending columns) every
+        // entry taken here lies in it, and an entry of a CSR that breaks the contract
+        // reads a wrong row of the chunk rather than memory outside it.
+        const uint32_t off = min(static_cast<uint32_t>(bcol[r] - kbase), static_cast<uint32_t>(kChunk - 1));
+        const uint32_t ent = (off << 16) | (bval[r] & 0xFFFFu);
+        // w times the X row of entry en
         auto add_entry = [&](uint32_t en) {
-          const bool ok = (en >> 16) < static_cast<uint32_t>(kChunk);
           const float w = to_f32<DT>(en & 0xFFFFu);
           const uint64_t w2 = ptx::f2_pack(w, w);
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (ok ? (en >> 16) : 0u) * (kCols * 2));
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (en >> 16) * (kCols * 2));
           const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
             const uint64_t x2 =
                 DT == 1 ? ptx::f2_pack(__uint_as_float(xw[h] << 16), __uint_as_float(xw[h] & 0xFFFF0000u))
                         : ptx::f2_pack(to_f32<DT>(xw[h] & 0xFFFFu), to_f32<DT>(xw[h] >> 16));
-            if (ok) acc[r][h] = ptx::f2_fma(w2, x2, acc[r][h]);
+            acc[r][h] = ptx::f2_fma(w2, x2, acc[r][h]);
           }
         };
         // two entries a turn, so that their shuffles and shared-memory reads overlap
