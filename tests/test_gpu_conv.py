@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 # ResNet-50 layers of the benchmark at its batch of 32)
 CASES = [(1, 5, 7, 64, 128), (2, 14, 14, 128, 256), (1, 28, 28, 64, 200), (3, 9, 30, 64, 64), (1, 3, 224, 64, 128),
          (1, 28, 28, 128, 200), (2, 9, 30, 256, 64), (3, 7, 7, 128, 128), (1, 11, 13, 64, 64),
+         (1, 1, 1, 128, 128), (2, 3, 5, 128, 64),
          (32, 28, 28, 128, 128), (32, 14, 14, 256, 256)]
 
 
