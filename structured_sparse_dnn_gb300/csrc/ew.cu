@@ -14,13 +14,15 @@
 //   k_tw_select  (shared with tile-wise) one CTA per row: exact top-k by radix
 //                select, ascending compaction, ties to the lower column;
 //   k_ew_values  the kept values' stored bits (k_ew_row_ptr: the row pointers);
-//   k_ew_spmm    one CTA per (32 rows, 256 columns), three per SM: the X panel
-//                streams through shared memory in 64-row chunks (double-buffered
-//                cp.async); each warp owns 4 rows and, for every kept entry of a row
-//                that falls in the chunk, adds w times the chunk's X row into 8 fp32
-//                accumulators per lane, held and updated as packed pairs (the entries
-//                of a row are held 32 at a time in registers, one per lane, and
-//                broadcast by one shuffle of the entry's chunk row and value bits).
+//   k_ew_spmm    one CTA of 16 warps per (64 rows, 256 columns), one per SM: the X
+//                panel streams through shared memory in 224-row chunks (two 112 KB
+//                buffers filled by cp.async; long chunks, because the handling of each
+//                (row, chunk) pair costs far more than an entry); each warp owns 4
+//                rows and, for every kept entry of a row that falls in the chunk,
+//                adds w times the chunk's X row into 8 fp32 accumulators per lane,
+//                held and updated as packed pairs (the entries of a row are held 32
+//                at a time in registers, one per lane, and broadcast by one shuffle
+//                of the entry's chunk row and value bits).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -35,11 +37,11 @@ cudaError_t launch_row_select(const float* scores, int64_t rows, int64_t K, cons
 
 namespace {
 
-constexpr int kRowsW = 4;                // output rows per warp
-constexpr int kRows = 8 * kRowsW;        // output rows per CTA
-constexpr int kCols = 256;               // output columns per CTA (8 per lane)
-constexpr int kChunk = 64;               // X rows per shared-memory chunk (32 KB)
-constexpr int kThreads = 256;
+constexpr int kRowsW = 4;                          // output rows per warp
+constexpr int kThreads = 512;
+constexpr int kRows = (kThreads / 32) * kRowsW;    // output rows per CTA
+constexpr int kCols = 256;                         // output columns per CTA (8 per lane)
+constexpr int kChunk = 224;                        // X rows per shared-memory chunk (112 KB)
 
 template <int DT>
 __global__ void __launch_bounds__(256) k_ew_mag(const uint8_t* __restrict__ W, int64_t M, int64_t K, int64_t ldw_b,
@@ -79,7 +81,7 @@ __device__ __forceinline__ float to_f32(uint32_t h) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, int64_t K,
+__global__ void __launch_bounds__(kThreads, 1) k_ew_spmm(int64_t M, int64_t N, int64_t K,
                                                          const int32_t* __restrict__ row_ptr,
                                                          const int32_t* __restrict__ col_idx,
                                                          const uint16_t* __restrict__ vals,
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_ew_spmm(int64_t M, int64_t N, i
 #pragma unroll
     for (int h = 0; h < 4; ++h) acc[r][h] = 0ull;
 
-  // chunk loader: 64 rows x 256 columns (32 KB) by 16-byte cp.async, zero past K / N
+  // chunk loader: kChunk rows x 256 columns by 16-byte cp.async, zero past K / N
   auto load_chunk = [&](int64_t c, int buf) {
     uint8_t* dst = smem + buf * (kChunk * kCols * 2);
     for (int q = threadIdx.x; q < kChunk * (kCols / 8); q += kThreads) {
