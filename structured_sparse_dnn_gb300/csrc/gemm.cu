@@ -988,6 +988,9 @@ __global__ void __launch_bounds__(Cfg<DT, SPARSE, GATHER, BN, MT, BROW, PAIR, BL
 }
 
 // ------------------------------------------------------------------ host side
+}  // namespace
+
+// (The tensor-map encoder and the 2-D map are shared with the other kernel files.)
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -1019,6 +1022,8 @@ bool make_map(CUtensorMap* m, const void* base, int eb, uint64_t cols, uint64_t 
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 // 4-D tensor map over NHWC activations seen innermost-first as (C, W, H, N),
 // one box = 64 channels x box_w columns x box_h rows x 1 image, 128B swizzle.

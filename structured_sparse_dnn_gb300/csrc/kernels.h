@@ -2,9 +2,15 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace ssdnn {
+
+// 2-D tensor map over a row-major matrix (rows x cols elements of eb bytes, pitch in
+// bytes, boxes of box_cols x box_rows); false if the driver refuses the encoding.
+bool make_map(CUtensorMap* m, const void* base, int eb, uint64_t cols, uint64_t rows, uint64_t pitch_bytes,
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz);
 
 // 2:4 magnitude prune + compress (one streaming pass over W).
 cudaError_t launch_sp24_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw, void* values,

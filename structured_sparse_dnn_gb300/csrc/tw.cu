@@ -10,9 +10,10 @@
 //
 // Three kernels:
 //   k_tw_score   one CTA per (tile, 128 consecutive k): stages the tile's 128 x
-//                128 block in shared memory with coalesced 16-byte loads, then one
-//                thread per k sums the rows in order (fp32), into the caller's
-//                workspace.
+//                128 block in shared memory (one TMA box, k_tw_score_tma, when W's
+//                base and pitch are 16-byte aligned; else 16-byte or element loads),
+//                then one thread per k sums the rows in order (fp32), into the
+//                caller's workspace.
 //   k_tw_select  one CTA per tile: exact top-L by a 4-pass 8-bit radix select on
 //                the score bits (non-negative floats order like their bits; each
 //                pass's digit found by one warp's scan of the histogram), then an
@@ -85,6 +86,60 @@ __global__ void __launch_bounds__(128) k_tw_score(const uint8_t* __restrict__ W,
 #pragma unroll 8
   for (int r = 0; r < rows; ++r) acc = acc + mag16<DT>(s_w[r][threadIdx.x]);
   scores[t * K + k] = acc;
+}
+
+// The same with the tile's 128 x 128 block brought in by one 2-D TMA box (rows past
+// M and columns past K arrive as zeros): the copy engine fetches the 32 KB without
+// the per-SM limit on 16-byte loads in flight that bounds the loop above.
+template <int DT>
+__global__ void __launch_bounds__(128) k_tw_score_tma(const __grid_constant__ CUtensorMap tmW, int64_t M, int64_t K,
+                                                      float* __restrict__ scores, uint32_t* err) {
+  __shared__ __align__(128) uint16_t s_w[128][128];
+  __shared__ __align__(8) uint64_t bar;
+  const int64_t t = blockIdx.y;
+  const int64_t kb = static_cast<int64_t>(blockIdx.x) * 128;
+  const int64_t r0 = t * 128;
+  const int rows = static_cast<int>(M - r0 < 128 ? M - r0 : 128);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(&bar, 128u * 128u * 2u);
+    ptx::tma_load_2d(&s_w[0][0], &tmW, &bar, static_cast<int32_t>(kb), static_cast<int32_t>(r0),
+                     ptx::policy_evict_normal());
+  }
+  if (!wait_bounded(&bar, 0, err)) {
+    wait_bounded(&bar, 0, nullptr);  // the copy may still be writing shared memory
+    return;
+  }
+  const int64_t k = kb + threadIdx.x;
+  if (k >= K) return;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int r = 0; r < rows; ++r) acc = acc + mag16<DT>(s_w[r][threadIdx.x]);
+  scores[t * K + k] = acc;
+}
+
+// The score pass: by TMA where W's base and pitch allow it (16-byte aligned), else by
+// 16-byte or element loads.
+cudaError_t launch_score(int dt, const uint8_t* w8, int64_t M, int64_t K, int64_t ldw_b, float* scores, int64_t nt,
+                         bool vec_ok, cudaStream_t s, uint32_t* err) {
+  const dim3 g(static_cast<unsigned>(ceil_div(K, 128)), static_cast<unsigned>(nt));
+  CUtensorMap m;
+  if (vec_ok && make_map(&m, w8, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(ldw_b),
+                         128, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    if (dt == SSDNN_BF16)
+      k_tw_score_tma<1><<<g, 128, 0, s>>>(m, M, K, scores, err);
+    else
+      k_tw_score_tma<0><<<g, 128, 0, s>>>(m, M, K, scores, err);
+  } else if (dt == SSDNN_BF16) {
+    k_tw_score<1><<<g, 128, 0, s>>>(w8, M, K, ldw_b, scores, vec_ok);
+  } else {
+    k_tw_score<0><<<g, 128, 0, s>>>(w8, M, K, ldw_b, scores, vec_ok);
+  }
+  return cudaGetLastError();
 }
 
 // Exclusive prefix sum over the block (whole warps, at most 1024 threads); returns
@@ -363,12 +418,7 @@ cudaError_t launch_bw_prune(int dt, const void* W, int64_t M, int64_t K, int64_t
   const auto* w8 = static_cast<const uint8_t*>(W);
   const bool vec_ok = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && ((ldw * 2) % 16 == 0);
   cudaError_t e;
-  dim3 g(static_cast<unsigned>(ceil_div(K, 128)), static_cast<unsigned>(tabs.nt));
-  if (dt == SSDNN_BF16)
-    k_tw_score<1><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
-  else
-    k_tw_score<0><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_score(dt, w8, M, K, ldw * 2, scores, tabs.nt, vec_ok, s, nullptr)) != cudaSuccess) return e;
   const int64_t nb_all = tabs.nt * (K / 64);
   k_bw_block_scores<<<static_cast<unsigned>(ceil_div(nb_all, 256)), 256, 0, s>>>(scores, K, tabs.nt, block_scores);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -399,18 +449,12 @@ cudaError_t launch_tw_prune(int dt, int tvw, const void* W, int64_t M, int64_t K
                             const TwTables& tabs, const int32_t* offsets, int32_t* indices,
                             const int32_t* schedule, void* packed, uint8_t* meta, uint8_t* meta_hw,
                             float* scores, cudaStream_t s, uint32_t* err) {
-  (void)err;
   if (tabs.nt == 0) return cudaSuccess;
   const auto* w8 = static_cast<const uint8_t*>(W);
   const bool vec_ok = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && ((ldw * 2) % 16 == 0);
   cudaError_t e;
   if (K > 0) {
-    dim3 g(static_cast<unsigned>(ceil_div(K, 128)), static_cast<unsigned>(tabs.nt));
-    if (dt == SSDNN_BF16)
-      k_tw_score<1><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
-    else
-      k_tw_score<0><<<g, 128, 0, s>>>(w8, M, K, ldw * 2, scores, vec_ok);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_score(dt, w8, M, K, ldw * 2, scores, tabs.nt, vec_ok, s, err)) != cudaSuccess) return e;
     k_tw_select<1024><<<static_cast<unsigned>(tabs.nt), 1024, 0, s>>>(scores, K, offsets, indices);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
