@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ew_spmm(int64_t M, int64_t N, i
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kCols;
   const int64_t nchunks = (K + kChunk - 1) / kChunk;
 
-  // this warp's 8 rows: next entry and end, and a register batch of the next 32
+  // this warp's kRowsW rows: next entry and end, and a register batch of the next 32
   // entries (lane l holds entry pos + l), refilled only when used up
   int32_t pos[kRowsW], end[kRowsW], bcol[kRowsW];
   uint32_t bval[kRowsW];
