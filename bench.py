@@ -468,7 +468,8 @@ def bench_rows(args, ss, dev, stream, flush, pk, d, wl, Wd, Xd, form_main) -> di
     eb = I.ELEM_BYTES[wl.dt]
     vb, mb, hb = ss.sp24_sizes(ss._DT[Wd.dtype], M, K)
     # a1: prune + compress (HBM bound): read W, write values + operand-order metadata
-    compress = lambda: ss.sp24_prune_compress(Wd, canonical_meta=False)
+    form_c = ss.sp24_prune_compress(Wd, canonical_meta=False)
+    compress = lambda: ss.sp24_prune_compress(Wd, canonical_meta=False, out=form_c)  # buffers reused
     t = statistics.mean(timed_steps(compress, steps, 2, flush, stream))
     tg = flushed_graph_ms(compress, flush, dev)
     nbytes = M * K * eb + vb + hb

@@ -169,11 +169,19 @@ class Sp24:
     meta_hw: torch.Tensor
 
 
-def sp24_prune_compress(W: torch.Tensor, canonical_meta: bool = True) -> Sp24:
-    """W (M x K, fp16/bf16/e4m3, CUDA) -> its 2:4-compressed form."""
+def sp24_prune_compress(W: torch.Tensor, canonical_meta: bool = True, out: Sp24 | None = None) -> Sp24:
+    """W (M x K, fp16/bf16/e4m3, CUDA) -> its 2:4-compressed form. `out`, a result of
+    an earlier call with the same shape and type, is overwritten in place (no
+    allocation; its canonical metadata too, if it has any)."""
     dt = _DT[W.dtype]
     M, K = W.shape
     assert W.stride(1) == 1
+    if out is not None:
+        if (out.dt, out.M, out.K) != (dt, M, K):
+            raise ValueError("sp24_prune_compress: out was made for another weight shape or type")
+        _check(lib.sp24_prune_compress(dt, _p(W), M, K, W.stride(0), _p(out.values), _p(out.meta), _p(out.meta_hw),
+                                       _stream(W.device)), "sp24_prune_compress")
+        return out
     vb, mb, hb = sp24_sizes(dt, M, K)
     Kp = (K + 31) // 32 * 32
     values = torch.empty((M, Kp // 2), dtype=W.dtype, device=W.device)

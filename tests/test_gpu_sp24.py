@@ -307,3 +307,25 @@ def test_sp24_gemm_host_buffers(copy_stream, rows_per_block):
     Y_ref = oracle.gemm.gemm_sp24(v_ref, m_ref, K, X, dt, dt)
     B = oracle.gemm.bound(oracle.sp24.decompress(v_ref, m_ref, K), X, dt)
     _check_y(Y_host, Y_ref, B, dt, REL[dt])
+
+
+@pytest.mark.parametrize("dt", ["bf16", "e4m3"])
+def test_compress_into_existing_result_matches_fresh(dt):
+    """out= overwrites an earlier 2:4 result in place: compressing a second weight into
+    the first weight's buffers gives exactly what a fresh call on it gives; a result of
+    another shape is refused before any device work."""
+    ss = lib()
+    M, K = 200, 520
+    W1 = dev_tensor(rand_bits(911, (M, K), dt, 0.5), dt)
+    W2 = dev_tensor(rand_bits(912, (M, K), dt, 0.5), dt)
+    form = ss.sp24_prune_compress(W1)
+    fresh = ss.sp24_prune_compress(W2)
+    again = ss.sp24_prune_compress(W2, out=form)
+    torch.cuda.synchronize()
+    assert ss.check_device_error() == 0
+    assert again is form
+    for name in ("values", "meta", "meta_hw"):
+        a, b = getattr(again, name), getattr(fresh, name)
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), name
+    with pytest.raises(ValueError):
+        ss.sp24_prune_compress(dev_tensor(rand_bits(913, (M, K + 32), dt, 0.5), dt), out=form)
