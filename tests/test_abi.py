@@ -218,3 +218,41 @@ def test_noalloc_refusals_host_only(ssdnn):
     st = lib.tw_prune_compress_noalloc(1, 0, 1 << 20, 256, K, K, keep.ctypes.data_as(P),
                                        2 << 20, 3 << 20, 4 << 20, 5 << 20, None, None, None)
     assert st == 2
+
+
+def test_out_refusals_come_before_any_library_call(ssdnn, monkeypatch):
+    """The prune helpers' out= forms refuse a result made for another shape, type,
+    kept counts or k (and a missing workspace) on the host, before any call into the
+    library: the library is replaced by an object that fails on any attribute access."""
+    import torch
+
+    class NoLib:
+        def __getattr__(self, name):
+            raise AssertionError(f"library called: {name}")
+
+    monkeypatch.setattr(ssdnn, "lib", NoLib())
+    t = torch.zeros(4, dtype=torch.uint8)
+    W = torch.zeros(256, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ssdnn.sp24_prune_compress(W, out=ssdnn.Sp24(ssdnn.BF16, 256, 544, t, None, t))
+    with pytest.raises(ValueError):
+        ssdnn.sp24_prune_compress(W, out=ssdnn.Sp24(ssdnn.F16, 256, 512, t, None, t))
+    keep = np.array([128, 64], dtype=np.int32)
+    tw = ssdnn.TileWise(ssdnn.BF16, True, 256, 512, keep, t, t, t, t, t, t)
+    with pytest.raises(ValueError):
+        ssdnn.tw_prune_compress(W, np.array([128, 68], dtype=np.int32), True, t, out=tw)
+    with pytest.raises(ValueError):
+        ssdnn.tw_prune_compress(W, keep, False, t, out=tw)
+    with pytest.raises(ValueError):
+        ssdnn.tw_prune_compress(W, keep, True, None, out=tw)
+    kb = np.array([2, 1], dtype=np.int32)
+    bw = ssdnn.BlockWise(ssdnn.BF16, 256, 512, kb, t, t, t, t)
+    with pytest.raises(ValueError):
+        ssdnn.bw_prune_compress(W, np.array([2, 2], dtype=np.int32), t, out=bw)
+    with pytest.raises(ValueError):
+        ssdnn.bw_prune_compress(W, kb, None, out=bw)
+    ew = ssdnn.ElementWise(ssdnn.BF16, 256, 512, 51, t, t, t, t, t)
+    with pytest.raises(ValueError):
+        ssdnn.ew_prune_compress(W, 52, t, out=ew)
+    with pytest.raises(ValueError):
+        ssdnn.ew_prune_compress(W, 51, None, out=ew)
